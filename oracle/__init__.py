@@ -1,0 +1,328 @@
+"""CPU oracle for the bitwise-deterministic routed-token grouped GEMM.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the benchmark's
+CPU-baseline / reference legs may import this package.  The product library
+(``bitwise_deterministic_moe_gb300``) never imports it, and this package never
+imports the product library: the two share no code, tables or constants.
+
+Contents and the passage each part follows:
+
+* ``routing`` -- the deterministic permutation of routed (token, choice)
+  entries into expert-contiguous rows.  Routing maps are order-sensitive data
+  ("NVIDIA fait passer le déterminisme bit à bit de Megatron Core à 2432 GPU
+  ...", section "Méthodologie de débogage du non-déterminisme"), so the order
+  is fixed: experts ascending, and inside an expert the flat index t*topk + j
+  ascending.  Plain definition: a stable sort by expert id (numpy's stable
+  argsort) and a bincount prefix.
+* ``expert_rows`` -- grouped GEMM, bf16 rounding, private-slot partials and
+  dprob, in binary64 (C, ``dmoe_oracle.c``), following "Trillion-Parameter
+  Pretraining Goes Bitwise-Deterministic: NVIDIA Cuts the Determinism Tax to
+  About 2%", section "Interpretation".
+* ``combine`` -- dprob[t, j] from the per-row values: a scatter through
+  row_src (the fixed-order slot combine reaches the plain dot product).
+* ``fingerprint`` -- chunk-wise tensor fingerprint with a header over dtype,
+  shape and numel (same French page, section "Méthodologie de débogage du
+  non-déterminisme": fingerprints computed on the GPU with shape, dtype and
+  element count recorded; chunk-wise for order-sensitive data).  Mode
+  "positional" hashes raw bits with position mixing; mode "xor" reduces each
+  chunk the way ``torch.hash_tensor`` reduces a tensor.
+
+The hash is this build's own definition (the pages name only the
+``torch.hash_tensor`` xor reduction):
+    fmix32  -- MurmurHash3's 32-bit finalizer (A. Appleby, public domain)
+    sm64    -- the splitmix64 output function (Steele, Lea, Flood 2014)
+    chunk c, words w_i (little-endian uint32, global word index i, zero-padded tail):
+        acc_c = sum_i fmix32(w_i ^ (i * 0x9E3779B9 mod 2^32))  mod 2^64
+        h_c   = sm64(acc_c ^ (c << 32) ^ chunk_len_bytes)
+    header: h = sm64(dtype_code); then h = sm64(h ^ v) for v in
+        (ndim, shape..., numel, nbytes)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "dmoe_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_build", "libdmoe_oracle.so")
+SLOT_WIDTH = 128   # columns per private dprob slot
+
+MASK64 = (1 << 64) - 1
+MASK32 = (1 << 32) - 1
+GOLDEN32 = 0x9E3779B9
+
+# dtype codes recorded in the fingerprint header (the library's ABI uses the
+# same numbering; it is an interface, written out separately on each side)
+DTYPE_CODES = {
+    "uint8": 0, "int8": 1, "int16": 2, "int32": 3, "int64": 4,
+    "float16": 5, "bfloat16": 6, "float32": 7, "float64": 8, "bool": 9,
+    "uint16": 10, "uint32": 11, "uint64": 12,
+}
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the C part of the oracle (gcc, -O2, no FP contraction, OpenMP)."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
+                               "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        i64 = ctypes.c_int64
+        ci = ctypes.c_int
+        lib.oracle_bf16_rne.argtypes = [ctypes.c_double]
+        lib.oracle_bf16_rne.restype = ctypes.c_uint16
+        lib.oracle_bf16_rne_array.argtypes = [P, i64, P]
+        lib.oracle_bf16_rne_array.restype = None
+        lib.oracle_expert_rows.argtypes = [P, P, P, P, P, i64, ci, ci, ci, ci, P, i64, ci, P, P, P, P]
+        lib.oracle_expert_rows.restype = ci
+        lib.oracle_dprob_from_output.argtypes = [P, P, P, i64, ci, ci, P, i64, ci, P, P]
+        lib.oracle_dprob_from_output.restype = None
+        lib.oracle_num_threads.argtypes = []
+        lib.oracle_num_threads.restype = ci
+        _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+# --------------------------------------------------------------------------
+# bf16 helpers (the oracle's own)
+# --------------------------------------------------------------------------
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns -> binary64 values (bf16 = upper half of a binary32)."""
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def bf16_rne(x) -> np.ndarray:
+    """binary64 -> bf16 bits, round to nearest even, from the IEEE rule (C)."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(x.shape, dtype=np.uint16)
+    _load().oracle_bf16_rne_array(_ptr(x), x.size, _ptr(out))
+    return out
+
+
+# --------------------------------------------------------------------------
+# routing
+# --------------------------------------------------------------------------
+def routing(topk_ids: np.ndarray, E: int):
+    """Deterministic permutation of routed entries into expert-contiguous rows.
+
+    Returns (expert_offsets int32 [E+1], row_src int32 [R]) where rows
+    [off[e], off[e+1]) belong to expert e and row_src[r] is the flat routing
+    index t*topk + j of permuted row r (ascending within each expert)."""
+    eid = np.asarray(topk_ids, dtype=np.int64).reshape(-1)
+    if eid.size and (eid.min() < 0 or eid.max() >= E):
+        raise ValueError("expert id out of range")
+    row_src = np.argsort(eid, kind="stable").astype(np.int32)
+    counts = np.bincount(eid, minlength=E)
+    off = np.zeros(E + 1, dtype=np.int64)
+    np.cumsum(counts, out=off[1:])
+    return off.astype(np.int32), row_src
+
+
+# --------------------------------------------------------------------------
+# grouped GEMM, slots, dprob (binary64, C)
+# --------------------------------------------------------------------------
+def expert_rows(X, W, off, rows, G=None, row_src=None, topk=1, want_Y=True, want_Yb=True,
+                want_P=False, want_D=False, slot_width=SLOT_WIDTH):
+    """Compute Y (binary64), Yb (bf16 bits), P [nrows,S] and D [nrows] for the
+    requested permuted rows.  X [R,K], W [E,N,K], G [T,N] are bf16 bit arrays."""
+    X = np.ascontiguousarray(X, dtype=np.uint16)
+    W = np.ascontiguousarray(W, dtype=np.uint16)
+    off = np.ascontiguousarray(off, dtype=np.int32)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    R, K = X.shape
+    E, N, K2 = W.shape
+    assert K2 == K and off.shape == (E + 1,)
+    S = (N + slot_width - 1) // slot_width
+    n = rows.size
+    Y = np.empty((n, N), np.float64) if want_Y else None
+    Yb = np.empty((n, N), np.uint16) if (want_Yb or want_D) else None
+    P = np.empty((n, S), np.float64) if want_P else None
+    D = np.empty((n,), np.float64) if want_D else None
+    if want_P or want_D:
+        G = np.ascontiguousarray(G, dtype=np.uint16)
+        row_src = np.ascontiguousarray(row_src, dtype=np.int32)
+    else:
+        G = None
+        row_src = None
+    rc = _load().oracle_expert_rows(_ptr(X), _ptr(W), _ptr(G), _ptr(off), _ptr(row_src),
+                                    R, E, K, N, int(topk), _ptr(rows), n, slot_width,
+                                    _ptr(Y), _ptr(Yb), _ptr(P), _ptr(D))
+    if rc != 0:
+        raise ValueError("a requested row is not covered by any expert")
+    return Y, Yb, P, D
+
+
+def dprob_from_output(G, expert_out, row_src, topk, rows=None, slot_width=SLOT_WIDTH):
+    """Slot partials P [nrows,S] and dots D [nrows] from a stored bf16 expert_out."""
+    G = np.ascontiguousarray(G, dtype=np.uint16)
+    Yb = np.ascontiguousarray(expert_out, dtype=np.uint16)
+    row_src = np.ascontiguousarray(row_src, dtype=np.int32)
+    R, N = Yb.shape
+    if rows is None:
+        rows = np.arange(R, dtype=np.int64)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    S = (N + slot_width - 1) // slot_width
+    P = np.empty((rows.size, S), np.float64)
+    D = np.empty((rows.size,), np.float64)
+    _load().oracle_dprob_from_output(_ptr(G), _ptr(Yb), _ptr(row_src), R, N, int(topk),
+                                     _ptr(rows), rows.size, slot_width, _ptr(P), _ptr(D))
+    return P, D
+
+
+def combine(D_rows, row_src, T, topk, rows=None):
+    """dprob [T, topk] (binary64) from per-row dots: dprob[row_src[r]] = D[r].
+    Entries of rows not requested are NaN."""
+    out = np.full(T * topk, np.nan, dtype=np.float64)
+    row_src = np.asarray(row_src)
+    if rows is None:
+        out[row_src] = D_rows
+    else:
+        out[row_src[np.asarray(rows)]] = D_rows
+    return out.reshape(T, topk)
+
+
+def full(inputs, slot_width=SLOT_WIDTH):
+    """Everything for a whole (small) problem: routing, Yb, P, dprob."""
+    cfg = inputs.cfg
+    off, row_src = routing(inputs.topk_ids, cfg.E)
+    rows = np.arange(cfg.R, dtype=np.int64)
+    Y, Yb, P, D = expert_rows(inputs.X, inputs.W, off, rows, G=inputs.G, row_src=row_src,
+                              topk=cfg.topk, want_Y=True, want_Yb=True, want_P=True, want_D=True,
+                              slot_width=slot_width)
+    dprob = combine(D, row_src, cfg.T, cfg.topk)
+    return dict(off=off, row_src=row_src, Y=Y, Yb=Yb, P=P, D=D, dprob=dprob)
+
+
+# --------------------------------------------------------------------------
+# fingerprint
+# --------------------------------------------------------------------------
+def fmix32(h: np.ndarray) -> np.ndarray:
+    h = np.asarray(h, dtype=np.uint32).copy()
+    h ^= h >> np.uint32(16)
+    h *= np.uint32(0x85EBCA6B)
+    h ^= h >> np.uint32(13)
+    h *= np.uint32(0xC2B2AE35)
+    h ^= h >> np.uint32(16)
+    return h
+
+
+def sm64(z: int) -> int:
+    z &= MASK64
+    z ^= z >> 30
+    z = (z * 0xBF58476D1CE4E5B9) & MASK64
+    z ^= z >> 27
+    z = (z * 0x94D049BB133111EB) & MASK64
+    z ^= z >> 31
+    return z
+
+
+def header_hash(dtype_code: int, shape) -> int:
+    shape = [int(s) for s in shape]
+    numel = 1
+    for s in shape:
+        numel *= s
+    nbytes = numel * _itemsize(dtype_code)
+    h = sm64(dtype_code)
+    for v in [len(shape)] + shape + [numel, nbytes]:
+        h = sm64(h ^ (v & MASK64))
+    return h
+
+
+_ITEMSIZE = {0: 1, 1: 1, 2: 2, 3: 4, 4: 8, 5: 2, 6: 2, 7: 4, 8: 8, 9: 1, 10: 2, 11: 4, 12: 8}
+
+
+def _itemsize(code: int) -> int:
+    return _ITEMSIZE[code]
+
+
+def num_chunks(nbytes: int, chunk_bytes: int) -> int:
+    return (nbytes + chunk_bytes - 1) // chunk_bytes
+
+
+def fingerprint_chunks(data: bytes | np.ndarray, chunk_bytes: int = 1 << 20) -> np.ndarray:
+    """Positional chunk hashes of a byte buffer (numpy, vectorised)."""
+    buf = np.frombuffer(memoryview(data).cast("B"), dtype=np.uint8) if not isinstance(data, np.ndarray) \
+        else np.ascontiguousarray(data).reshape(-1).view(np.uint8)
+    nbytes = buf.size
+    assert chunk_bytes % 4 == 0 and chunk_bytes > 0
+    nch = num_chunks(nbytes, chunk_bytes)
+    out = np.zeros(nch, dtype=np.uint64)
+    wpc = chunk_bytes // 4
+    for c in range(nch):
+        b0 = c * chunk_bytes
+        b1 = min(nbytes, b0 + chunk_bytes)
+        seg = buf[b0:b1]
+        pad = (-seg.size) % 4
+        if pad:
+            seg = np.concatenate([seg, np.zeros(pad, np.uint8)])
+        w = seg.view("<u4").astype(np.uint32)
+        i = (np.arange(w.size, dtype=np.uint64) + np.uint64(c * wpc))
+        key = ((i * np.uint64(GOLDEN32)) & np.uint64(MASK32)).astype(np.uint32)
+        acc = int(fmix32(w ^ key).astype(np.uint64).sum(dtype=np.uint64))
+        out[c] = sm64(acc ^ ((c << 32) & MASK64) ^ (b1 - b0))
+    return out
+
+
+_XOR_KIND = {0: "u", 1: "i", 2: "i", 3: "i", 4: "i", 5: "f", 6: "bf", 7: "f", 8: "f", 9: "u", 10: "u",
+             11: "u", 12: "u"}
+_NP_DTYPE = {0: np.uint8, 1: np.int8, 2: np.int16, 3: np.int32, 4: np.int64, 5: np.float16, 6: np.uint16,
+             7: np.float32, 8: np.float64, 9: np.uint8, 10: np.uint16, 11: np.uint32, 12: np.uint64}
+
+
+def xor_chunks(data: np.ndarray, dtype_code: int, chunk_bytes: int = 1 << 20) -> np.ndarray:
+    """Per-chunk xor of the elements widened to 64 bits (floats to binary64
+    bit patterns, signed integers sign-extended, unsigned zero-extended)."""
+    es = _itemsize(dtype_code)
+    assert chunk_bytes % es == 0
+    a = np.ascontiguousarray(data).reshape(-1).view(np.uint8).view(_NP_DTYPE[dtype_code])
+    kind = _XOR_KIND[dtype_code]
+    if kind == "f":
+        w = a.astype(np.float64).view(np.uint64)
+    elif kind == "bf":
+        w = bf16_to_f64(a).view(np.uint64)
+    elif kind == "i":
+        w = a.astype(np.int64).view(np.uint64)
+    else:
+        w = a.astype(np.uint64)
+    per = chunk_bytes // es
+    nch = num_chunks(a.size * es, chunk_bytes)
+    out = np.zeros(nch, dtype=np.uint64)
+    for c in range(nch):
+        out[c] = np.bitwise_xor.reduce(w[c * per:(c + 1) * per]) if w[c * per:(c + 1) * per].size else 0
+    return out
+
+
+def fingerprint(arr: np.ndarray, dtype_code: int, shape=None, chunk_bytes: int = 1 << 20, mode: str = "positional"):
+    """(chunk hashes uint64 [nchunks], header hash) of an array's raw bytes."""
+    arr = np.ascontiguousarray(arr)
+    if shape is None:
+        shape = arr.shape
+    if mode == "positional":
+        ch = fingerprint_chunks(arr, chunk_bytes)
+    elif mode == "xor":
+        ch = xor_chunks(arr, dtype_code, chunk_bytes)
+    else:
+        raise ValueError(mode)
+    return ch, header_hash(dtype_code, shape)
