@@ -1,0 +1,451 @@
+"""Benchmark of the bitwise-deterministic MoE grouped GEMM + dprob path on GB300.
+
+One step = one pass of the whole hot path over one batch of seeded synthetic
+routed tokens shaped like the LatentMoE layer (T=8192 tokens, 512 experts,
+top-22, K=1024, N=2048 latent, Zipf(1.1) expert popularity):
+  1. routing indices (dmoe_permute_indices)
+  2. chunk fingerprint of the routing map row_src (order-sensitive data)
+  3. grouped GEMM with the fused private-slot dprob epilogue + fixed-order
+     combine (moe_grouped_gemm_dprob)
+  4. chunk fingerprint of dprob
+The metric is algorithmic grouped-GEMM TFLOP/s (2*R*K*N per step) over the
+whole step time.  The determinism tax compares the deterministic GEMM call
+with the atomicAdd control (memset + moe_grouped_gemm_dprob_atomic).
+
+Usage: python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+For N > 1 (torchrun) every rank runs an independent replica on its own GPU
+(the path has no data exchange on one node); value = all ranks' flops / the
+slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from bitwise_deterministic_moe_gb300 import synth  # noqa: E402
+
+WORKLOAD = "latent"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "grouped_gemm_latent_traffic.txt")
+
+
+def peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return p, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def algorithmic(cfg, off):
+    """Algorithmic flops and HBM bytes of one grouped-GEMM+dprob call."""
+    counts = np.diff(off)
+    used = int((counts > 0).sum())
+    R, K, N, T, S = cfg.R, cfg.K, cfg.N, cfg.T, cfg.S
+    flops = 2.0 * R * K * N
+    bytes_ = (R * K * 2 + used * N * K * 2 + R * N * 2 + T * N * 2 + 2 * S * R * 4 + R * 4 + R * 4
+              + (cfg.E + 1) * 4)
+    return flops, bytes_
+
+
+def gemm_traffic_per_launch():
+    """dram read+write bytes of the GEMM kernel from the committed ncu summary,
+    or None when the kernel source changed after the capture."""
+    try:
+        import hashlib
+        kv = {}
+        for line in open(TRAFFIC_FILE):
+            if "=" in line and not line.startswith("#"):
+                k, v = line.split("=", 1)
+                kv[k.strip()] = v.strip()
+        src = os.path.join(ROOT, "bitwise_deterministic_moe_gb300", "csrc", "grouped_gemm.cu")
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if kv.get("kernel_source_sha256_16") != h:
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+def cpu_baseline(cfg, inp, target_s=12.0):
+    """The oracle as it stands, timed on this host's cores on a bounded sample
+    of rows of the same workload (GEMM + bf16 rounding + slot partials + dprob)."""
+    import oracle
+    off, src = oracle.routing(inp.topk_ids, cfg.E)
+    rng = np.random.default_rng(7)
+    n = 64
+    t = 0.0
+    while True:
+        rows = np.sort(rng.choice(cfg.R, n, replace=False)).astype(np.int64)
+        t0 = time.perf_counter()
+        oracle.expert_rows(inp.X, inp.W, off, rows, G=inp.G, row_src=src, topk=cfg.topk, want_Y=False,
+                           want_Yb=True, want_P=True, want_D=True)
+        t = time.perf_counter() - t0
+        if t >= target_s * 0.5 or n >= cfg.R:
+            break
+        n = min(cfg.R, int(n * max(2.0, min(16.0, target_s / max(t, 1e-3)))))
+    flops = 2.0 * n * cfg.K * cfg.N
+    return {"value": flops / t / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{n} of {cfg.R} permuted rows of the {cfg.name} workload (GEMM+bf16+slots+dprob, fp64), "
+                      f"{t:.1f} s"}
+
+
+def run_reference(args):
+    """Reference arm: the oracle (the only reference this path has) on the host
+    cores, each step a bounded sample of the workload."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    cfg = synth.CONFIGS[args.config]
+    inp = synth.make_inputs(cfg)
+    import oracle
+    off, src = oracle.routing(inp.topk_ids, cfg.E)
+    rows_per_step = args.ref_rows
+    rng = np.random.default_rng(11)
+    samples = [np.sort(rng.choice(cfg.R, rows_per_step, replace=False)).astype(np.int64)
+               for _ in range(args.warmup + args.steps)]
+    for i in range(args.warmup):
+        oracle.expert_rows(inp.X, inp.W, off, samples[i], G=inp.G, row_src=src, topk=cfg.topk, want_Y=False,
+                           want_Yb=True, want_P=True, want_D=True)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle.routing(inp.topk_ids, cfg.E)
+        oracle.expert_rows(inp.X, inp.W, off, samples[args.warmup + i], G=inp.G, row_src=src, topk=cfg.topk,
+                           want_Y=False, want_Yb=True, want_P=True, want_D=True)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows_per_step * cfg.K * cfg.N * args.steps
+    value = flops / dt / 1e12
+    line = {
+        "impl": "reference", "metric": "grouped-GEMM+dprob TFLOP/s", "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{cfg.name}: T={cfg.T} E={cfg.E} topk={cfg.topk} K={cfg.K} N={cfg.N} "
+                               f"routing={cfg.routing}", "rows_per_step": rows_per_step},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": f"{rows_per_step} of {cfg.R} permuted rows per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("gloo")
+    cfg = synth.CONFIGS[args.config]
+
+    # the oracle's CPU baseline runs before any GPU work (rank 0, N = 1 only)
+    inp = synth.make_inputs(cfg)
+    base = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        base = cpu_baseline(cfg, inp, target_s=args.cpu_seconds)
+
+    from bitwise_deterministic_moe_gb300 import api, build
+    build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    api.load()
+
+    def bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+
+    h_ids = torch.from_numpy(inp.topk_ids).pin_memory()
+    h_X = bf16(inp.X).pin_memory()
+    h_W = bf16(inp.W).pin_memory()
+    h_G = bf16(inp.G).pin_memory()
+    ids = h_ids.to(dev)
+    X = h_X.to(dev)
+    W = h_W.to(dev)
+    G = h_G.to(dev)
+    R, S, T, k = cfg.R, cfg.S, cfg.T, cfg.topk
+    ws = api.workspace(T, k, cfg.E, dev)
+    off = torch.empty(cfg.E + 1, dtype=torch.int32, device=dev)
+    src = torch.empty(R, dtype=torch.int32, device=dev)
+    out = torch.empty(R, cfg.N, dtype=torch.bfloat16, device=dev)
+    slots = torch.empty(S, R, dtype=torch.float32, device=dev)
+    dprob = torch.empty(T, k, dtype=torch.float32, device=dev)
+    fp_src = torch.empty(api.fingerprint_num_chunks(R * 4), dtype=torch.int64, device=dev)
+    fp_dp = torch.empty(api.fingerprint_num_chunks(R * 4), dtype=torch.int64, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    launches_per_step = 4 + 2 + 2 + 2   # routing 4, fingerprint 2, GEMM + combine 2, fingerprint 2
+
+    def step(ev=None):
+        api.permute_indices(ids, cfg.E, ws, off, src)
+        api.fingerprint(src, out=fp_src)
+        if ev is not None:
+            ev[0].record(stream)
+        api.grouped_gemm_dprob(X, W, off, G, src, k, ws, out=out, slots=slots, dprob=dprob)
+        if ev is not None:
+            ev[1].record(stream)
+        api.fingerprint(dprob, out=fp_dp)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    st = api.read_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {st} after warm-up")
+    off_np = off.cpu().numpy()
+    flops, abytes = algorithmic(cfg, off_np)
+
+    # ---------------- timed region: K steps, inputs resident in HBM (> L2)
+    gemm_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(gemm_ev[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    ms = t_start.elapsed_time(t_end)
+    gemm_ms = float(np.mean([a.elapsed_time(b) for a, b in gemm_ev]))
+    if api.read_status(ws) != 0:
+        raise RuntimeError("device status set during the timed region")
+    ms_max = ms
+    if world > 1:
+        tt = torch.tensor([ms], dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_max = float(tt.item())
+    ms_per_step = ms_max / args.steps
+    value = world * flops * args.steps / (ms_max * 1e-3) / 1e12
+
+    # ---------------- determinism tax: deterministic call vs atomic control
+    def timed(fn, iters):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        fn()
+        torch.cuda.synchronize(dev)
+        a.record(stream)
+        for _ in range(iters):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / iters
+
+    dprob_a = torch.empty_like(dprob)
+    tax = {}
+    for name in (args.config, "imbal"):
+        if name == args.config:
+            tX, tW, tG, toff, tsrc, tcfg, tws = X, W, G, off, src, cfg, ws
+        else:
+            if args.skip_imbal:
+                continue
+            tcfg = synth.CONFIGS[name]
+            ti = synth.make_inputs(tcfg)
+            tX, tW, tG = bf16(ti.X).to(dev), bf16(ti.W).to(dev), bf16(ti.G).to(dev)
+            tws = api.workspace(tcfg.T, tcfg.topk, tcfg.E, dev)
+            toff, tsrc = api.permute_indices(torch.from_numpy(ti.topk_ids).to(dev), tcfg.E, tws)
+        to = torch.empty(tcfg.R, tcfg.N, dtype=torch.bfloat16, device=dev)
+        tsl = torch.empty(tcfg.S, tcfg.R, dtype=torch.float32, device=dev)
+        tdp = torch.empty(tcfg.T, tcfg.topk, dtype=torch.float32, device=dev)
+        tda = torch.empty_like(tdp)
+        det_ms, atom_ms = [], []
+        for _ in range(3):   # interleave to share clock/thermal conditions
+            det_ms.append(timed(lambda: api.grouped_gemm_dprob(tX, tW, toff, tG, tsrc, tcfg.topk, tws, out=to,
+                                                               slots=tsl, dprob=tdp), args.tax_iters))
+            atom_ms.append(timed(lambda: api.grouped_gemm_dprob_atomic(tX, tW, toff, tG, tsrc, tcfg.topk, tws,
+                                                                       out=to, dprob=tda), args.tax_iters))
+        d, a = float(np.median(det_ms)), float(np.median(atom_ms))
+        tf, _ = algorithmic(tcfg, toff.cpu().numpy())
+        tax[name] = {"det_ms": d, "atomic_ms": a, "tax_pct": (d / a - 1.0) * 100.0,
+                     "det_tflops": tf / (d * 1e-3) / 1e12}
+        if name != args.config:
+            del tX, tW, tG, to, tsl, tdp, tda
+            torch.cuda.empty_cache()
+    del dprob_a
+
+    # ---------------- end to end through the public API, host buffers
+    e2e = None
+    if not args.skip_e2e:
+        h_dprob = torch.empty(T, k, dtype=torch.float32).pin_memory()
+        h_fp = torch.empty_like(fp_dp, device="cpu").pin_memory()
+        h_fps = torch.empty_like(fp_src, device="cpu").pin_memory()
+
+        def e2e_step():
+            ids.copy_(h_ids, non_blocking=True)
+            X.copy_(h_X, non_blocking=True)
+            W.copy_(h_W, non_blocking=True)
+            G.copy_(h_G, non_blocking=True)
+            step()
+            h_dprob.copy_(dprob, non_blocking=True)
+            h_fp.copy_(fp_dp, non_blocking=True)
+            h_fps.copy_(fp_src, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = a.elapsed_time(b)
+        if world > 1:
+            tt = torch.tensor([e_ms], dtype=torch.float64)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e_ms = float(tt.item())
+        h2d = sum(t.numel() * t.element_size() for t in (h_ids, h_X, h_W, h_G))
+        d2h = sum(t.numel() * t.element_size() for t in (h_dprob, h_fp, h_fps))
+        e2e = {"value": world * flops * args.e2e_steps / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": e_ms / args.e2e_steps}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    pk, pk_kind = peaks()
+    gemm_s = gemm_ms * 1e-3
+    achieved_gbs = abytes / gemm_s / 1e9
+    achieved_tf = flops / gemm_s / 1e12
+    t_hbm = abytes / (pk["hbm_gbs"] * 1e9)
+    t_tc = flops / (pk["bf16_tflops"] * 1e12)
+    traffic = gemm_traffic_per_launch()
+    if t_hbm >= t_tc:
+        roof = {"bound": "hbm", "achieved": achieved_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved_gbs / pk["hbm_gbs"], "traffic": traffic}
+    else:
+        roof = {"bound": "tensor", "achieved": achieved_tf, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved_tf / pk["bf16_tflops"], "traffic": traffic}
+    roof.update({"kernel": "grouped_gemm_kernel<slots> + combine (moe_grouped_gemm_dprob)",
+                 "launch_ms": gemm_ms, "algorithmic_bytes": abytes, "algorithmic_flops": flops,
+                 "peak_source": f"{pk_kind} ({PEAKS_FILE if pk_kind == 'measured' else 'profiling recipe'})",
+                 "tensor_frac": achieved_tf / pk["bf16_tflops"], "tensor_tflops": achieved_tf,
+                 "hbm_frac": achieved_gbs / pk["hbm_gbs"]})
+    line = {
+        "metric": "grouped-GEMM+dprob TFLOP/s", "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{cfg.name}: T={cfg.T} E={cfg.E} topk={cfg.topk} K={cfg.K} N={cfg.N} "
+                               f"routing={cfg.routing} (seed {cfg.seed})",
+                   "step": "permute + fingerprint(row_src) + grouped GEMM/slot dprob/combine + fingerprint(dprob)",
+                   "l2": "inputs larger than L2 (X+W+grad_out = %.2f GB)" % ((cfg.R * cfg.K + cfg.E * cfg.N * cfg.K
+                                                                            + cfg.T * cfg.N) * 2 / 1e9),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "maxvio": synth.maxvio(inp.topk_ids, cfg.E)},
+        "gpu_launches": launches_per_step * args.steps,
+        "roofline": roof,
+        "determinism_tax": tax,
+        "e2e": e2e,
+        "clocks": clocks,
+    }
+    if base is not None:
+        line["cpu_baseline"] = base
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default=WORKLOAD, choices=sorted(synth.CONFIGS))
+    ap.add_argument("--tax-iters", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-rows", type=int, default=1024)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--skip-imbal", action="store_true")
+    ap.add_argument("--skip-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

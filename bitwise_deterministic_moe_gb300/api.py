@@ -1,0 +1,282 @@
+"""Thin ctypes binding of libdmoe.so (C ABI in include/dmoe.h).
+
+Argument marshalling only: every step of the computation runs in the
+library's CUDA kernels.  Tensors must be CUDA tensors on the current device;
+calls are enqueued on torch's current stream and are asynchronous.  torch
+provides device memory and streams, nothing else.
+
+If the library has not been built, the first call raises -- there is no CPU
+fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+from . import build as _build
+
+SLOT_COLS = 128
+MAX_EXPERTS = 1024
+
+OK = 0
+STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "invalid routing data",
+                4: "device wait timed out", 5: "CUDA error", 6: "workspace missing or too small"}
+
+DTYPE_CODES = {
+    torch.uint8: 0, torch.int8: 1, torch.int16: 2, torch.int32: 3, torch.int64: 4,
+    torch.float16: 5, torch.bfloat16: 6, torch.float32: 7, torch.float64: 8, torch.bool: 9,
+}
+for _name, _code in (("uint16", 10), ("uint32", 11), ("uint64", 12)):
+    if hasattr(torch, _name):
+        DTYPE_CODES[getattr(torch, _name)] = _code
+
+
+class DmoeError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)} (status {status})")
+        self.status = status
+
+
+class _Launch(ctypes.Structure):
+    _fields_ = [("num_ctas", ctypes.c_int), ("reserved", ctypes.c_int)]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load() -> ctypes.CDLL:
+    """Load libdmoe.so; raises if it is missing (build it with build.build())."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if not os.path.exists(path):
+        raise ImportError(f"libdmoe.so is not built ({path}); run bitwise_deterministic_moe_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    P, I, SZ, U64P = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.POINTER(ctypes.c_uint64)
+    LP = ctypes.POINTER(_Launch)
+    sig = {
+        "dmoe_status_string": ([I], ctypes.c_char_p),
+        "dmoe_version": ([], I),
+        "dmoe_workspace_bytes": ([I, I, I], SZ),
+        "dmoe_read_status": ([P, P], I),
+        "dmoe_permute_indices": ([P, I, I, I, P, P, P, SZ, P], I),
+        "moe_grouped_gemm_fwd": ([P, P, P, I, I, I, I, P, LP, P, SZ, P], I),
+        "moe_grouped_gemm_dprob": ([P, P, P, I, I, I, I, P, P, P, I, I, P, P, LP, P, SZ, P], I),
+        "moe_grouped_gemm_dprob_atomic": ([P, P, P, I, I, I, I, P, P, P, I, I, P, LP, P, SZ, P], I),
+        "moe_dprob_epilogue": ([P, P, P, P, I, I, I, I, I, P, P], I),
+        "moe_dprob_combine": ([P, P, I, I, I, I, P, P], I),
+        "dmoe_fingerprint_num_chunks": ([SZ, SZ], SZ),
+        "dmoe_fingerprint": ([P, SZ, I, I, ctypes.POINTER(ctypes.c_int64), SZ, I, P, U64P, P], I),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = lib
+    return lib
+
+
+def _stream(stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _check(st: int, what: str):
+    if st != OK:
+        raise DmoeError(st, what)
+
+
+def _need(t: torch.Tensor, dtype, name: str, shape=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _launch(num_ctas: int):
+    return ctypes.byref(_Launch(int(num_ctas), 0))
+
+
+# ------------------------------------------------------------------ workspace
+def workspace_bytes(T: int, topk: int, E: int) -> int:
+    return int(load().dmoe_workspace_bytes(T, topk, E))
+
+
+def workspace(T: int, topk: int, E: int, device=None) -> torch.Tensor:
+    """Zero-filled device workspace for a problem of this size."""
+    n = workspace_bytes(T, topk, E)
+    return torch.zeros(n, dtype=torch.uint8, device=device or torch.cuda.current_device())
+
+
+def read_status(ws: torch.Tensor, stream=None) -> int:
+    """Synchronise, return and clear the device status word (0 = ok)."""
+    return int(load().dmoe_read_status(_ptr(ws), _stream(stream)))
+
+
+# ------------------------------------------------------------------ routing
+def permute_indices(topk_ids: torch.Tensor, E: int, ws: torch.Tensor,
+                    expert_offsets: Optional[torch.Tensor] = None, row_src: Optional[torch.Tensor] = None,
+                    stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    _need(topk_ids, torch.int32, "topk_ids")
+    T, topk = topk_ids.shape
+    dev = topk_ids.device
+    if expert_offsets is None:
+        expert_offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    if row_src is None:
+        row_src = torch.empty(T * topk, dtype=torch.int32, device=dev)
+    _need(expert_offsets, torch.int32, "expert_offsets", (E + 1,))
+    _need(row_src, torch.int32, "row_src", (T * topk,))
+    st = load().dmoe_permute_indices(_ptr(topk_ids), T, topk, E, _ptr(expert_offsets), _ptr(row_src),
+                                     _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "dmoe_permute_indices")
+    return expert_offsets, row_src
+
+
+# ------------------------------------------------------------------ GEMM
+def _gemm_shapes(X, W, offs):
+    _need(X, torch.bfloat16, "X_perm")
+    _need(W, torch.bfloat16, "W")
+    _need(offs, torch.int32, "expert_offsets")
+    R, K = X.shape
+    E, N, K2 = W.shape
+    if K2 != K:
+        raise ValueError("X_perm and W disagree on K")
+    if offs.shape != (E + 1,):
+        raise ValueError("expert_offsets must have E+1 entries")
+    return R, E, K, N
+
+
+def grouped_gemm_fwd(X_perm, W, expert_offsets, ws, out=None, num_ctas: int = 0, stream=None):
+    R, E, K, N = _gemm_shapes(X_perm, W, expert_offsets)
+    if out is None:
+        out = torch.empty(R, N, dtype=torch.bfloat16, device=X_perm.device)
+    _need(out, torch.bfloat16, "expert_out", (R, N))
+    st = load().moe_grouped_gemm_fwd(_ptr(X_perm), _ptr(W), _ptr(expert_offsets), R, E, K, N, _ptr(out),
+                                     _launch(num_ctas), _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "moe_grouped_gemm_fwd")
+    return out
+
+
+def grouped_gemm_dprob(X_perm, W, expert_offsets, grad_out, row_src, topk: int, ws, out=None, slots=None,
+                       dprob=None, num_ctas: int = 0, stream=None):
+    """Deterministic path: returns (expert_out bf16 [R,N], dprob fp32 [T,topk], slots fp32 [S,R])."""
+    R, E, K, N = _gemm_shapes(X_perm, W, expert_offsets)
+    T = R // topk
+    dev = X_perm.device
+    S = N // SLOT_COLS
+    if out is None:
+        out = torch.empty(R, N, dtype=torch.bfloat16, device=dev)
+    if slots is None:
+        slots = torch.empty(S, R, dtype=torch.float32, device=dev)
+    if dprob is None:
+        dprob = torch.empty(T, topk, dtype=torch.float32, device=dev)
+    _need(out, torch.bfloat16, "expert_out", (R, N))
+    _need(grad_out, torch.bfloat16, "grad_out", (T, N))
+    _need(row_src, torch.int32, "row_src", (R,))
+    _need(slots, torch.float32, "slots", (S, R))
+    _need(dprob, torch.float32, "dprob", (T, topk))
+    st = load().moe_grouped_gemm_dprob(_ptr(X_perm), _ptr(W), _ptr(expert_offsets), R, E, K, N, _ptr(out),
+                                       _ptr(grad_out), _ptr(row_src), T, topk, _ptr(slots), _ptr(dprob),
+                                       _launch(num_ctas), _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "moe_grouped_gemm_dprob")
+    return out, dprob, slots
+
+
+def grouped_gemm_dprob_atomic(X_perm, W, expert_offsets, grad_out, row_src, topk: int, ws, out=None, dprob=None,
+                              num_ctas: int = 0, stream=None):
+    """Nondeterministic atomicAdd control: returns (expert_out, dprob)."""
+    R, E, K, N = _gemm_shapes(X_perm, W, expert_offsets)
+    T = R // topk
+    dev = X_perm.device
+    if out is None:
+        out = torch.empty(R, N, dtype=torch.bfloat16, device=dev)
+    if dprob is None:
+        dprob = torch.empty(T, topk, dtype=torch.float32, device=dev)
+    _need(out, torch.bfloat16, "expert_out", (R, N))
+    _need(grad_out, torch.bfloat16, "grad_out", (T, N))
+    _need(row_src, torch.int32, "row_src", (R,))
+    _need(dprob, torch.float32, "dprob", (T, topk))
+    st = load().moe_grouped_gemm_dprob_atomic(_ptr(X_perm), _ptr(W), _ptr(expert_offsets), R, E, K, N, _ptr(out),
+                                              _ptr(grad_out), _ptr(row_src), T, topk, _ptr(dprob),
+                                              _launch(num_ctas), _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "moe_grouped_gemm_dprob_atomic")
+    return out, dprob
+
+
+def dprob_epilogue(grad_out, expert_out, expert_offsets, row_src, topk: int, slots=None, stream=None):
+    _need(expert_out, torch.bfloat16, "expert_out")
+    R, N = expert_out.shape
+    T = R // topk
+    E = expert_offsets.numel() - 1
+    S = N // SLOT_COLS
+    if slots is None:
+        slots = torch.empty(S, R, dtype=torch.float32, device=expert_out.device)
+    _need(grad_out, torch.bfloat16, "grad_out", (T, N))
+    _need(expert_offsets, torch.int32, "expert_offsets")
+    _need(row_src, torch.int32, "row_src", (R,))
+    _need(slots, torch.float32, "slots", (S, R))
+    st = load().moe_dprob_epilogue(_ptr(grad_out), _ptr(expert_out), _ptr(expert_offsets), _ptr(row_src), R, E, T,
+                                   topk, N, _ptr(slots), _stream(stream))
+    _check(st, "moe_dprob_epilogue")
+    return slots
+
+
+def dprob_combine(slots, row_src, topk: int, dprob=None, stream=None):
+    _need(slots, torch.float32, "slots")
+    S, R = slots.shape
+    T = R // topk
+    if dprob is None:
+        dprob = torch.empty(T, topk, dtype=torch.float32, device=slots.device)
+    _need(row_src, torch.int32, "row_src", (R,))
+    _need(dprob, torch.float32, "dprob", (T, topk))
+    st = load().moe_dprob_combine(_ptr(slots), _ptr(row_src), R, S, T, topk, _ptr(dprob), _stream(stream))
+    _check(st, "moe_dprob_combine")
+    return dprob
+
+
+# ------------------------------------------------------------------ fingerprint
+def fingerprint_num_chunks(nbytes: int, chunk_bytes: int = 1 << 20) -> int:
+    return int(load().dmoe_fingerprint_num_chunks(nbytes, chunk_bytes))
+
+
+def fingerprint(t: torch.Tensor, chunk_bytes: int = 1 << 20, mode: int = 0, out=None, stream=None):
+    """Chunk-wise fingerprint of a contiguous CUDA tensor's bytes.
+
+    Returns (chunk hashes as an int64 tensor holding uint64 bit patterns, header
+    hash as a Python int)."""
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError("fingerprint needs a contiguous CUDA tensor")
+    code = DTYPE_CODES[t.dtype]
+    nbytes = t.numel() * t.element_size()
+    nch = fingerprint_num_chunks(nbytes, chunk_bytes)
+    if out is None:
+        out = torch.empty(max(nch, 1), dtype=torch.int64, device=t.device)
+    shape = (ctypes.c_int64 * max(t.dim(), 1))(*t.shape)
+    header = ctypes.c_uint64(0)
+    st = load().dmoe_fingerprint(_ptr(t) if nbytes else None, nbytes, code, t.dim(), shape, chunk_bytes, mode,
+                                 _ptr(out), ctypes.byref(header), _stream(stream))
+    _check(st, "dmoe_fingerprint")
+    return out[:nch], int(header.value)
+
+
+def fingerprint_host(t: torch.Tensor, chunk_bytes: int = 1 << 20, mode: int = 0):
+    """Fingerprint, returned as (list of Python ints, header int) after a sync."""
+    ch, h = fingerprint(t, chunk_bytes, mode)
+    vals = [v & ((1 << 64) - 1) for v in ch.cpu().tolist()]
+    return vals, h

@@ -1,0 +1,405 @@
+// Persistent grouped GEMM for GB300 (sm_103a) with the fused private-slot
+// dprob epilogue.
+//
+// The operation follows "Trillion-Parameter Pretraining Goes Bitwise-
+// Deterministic: NVIDIA Cuts the Determinism Tax to About 2%", section
+// "Interpretation": in the grouped-GEMM epilogue every N-tile used to add its
+// share of dprob[token] at one address, so the result depended on arrival
+// order; here each N-tile writes its share into a private slot and a later
+// pass combines the slots in a fixed order.  The slot width is fixed at 128
+// output columns, independent of the MMA tile width, so the bits do not
+// depend on the tile shape either.
+//
+// Design (one CTA per SM, persistent, warp-specialised, 192 threads):
+//   warp 0  TMA producer: A tile [128 rows x 64 k] and B tile [256 n x 64 k]
+//           per stage, 128-byte swizzle, 4-stage ring in shared memory.
+//   warp 1  tcgen05.mma issuer (one thread): 128x256x16 bf16 MMAs, fp32
+//           accumulators in tensor memory, double-buffered (2 x 256 columns).
+//   warps 2-5  epilogue: tcgen05.ld of the accumulator, bf16 rounding, masked
+//           stores of expert_out rows, and the per-slot dot products with
+//           grad_out in the fixed tree (one thread per output row).
+// Tiles are enumerated expert-major, then n-tile, then m-tile, and dealt out
+// round-robin to the CTAs: each output element is produced by exactly one
+// tile with a fixed k order, so the result does not depend on the grid size.
+// An M-tile may run past its expert's last row into the next expert's rows;
+// those rows are computed but never stored.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace dmoe {
+namespace {
+
+constexpr int BM = 128;                  // rows per tile (UMMA M)
+constexpr int BN = 256;                  // columns per tile (UMMA N)
+constexpr int BK = 64;                   // k per stage: one 128-byte swizzle row of bf16
+constexpr int UMMA_K = 16;               // k per tcgen05.mma (kind::f16)
+constexpr int STAGES = 4;
+constexpr int A_STAGE_BYTES = BM * BK * 2;
+constexpr int B_STAGE_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int ACC_BUFS = 2;
+constexpr int TMEM_COLS = ACC_BUFS * BN;  // 512 = all of tensor memory
+constexpr int NUM_THREADS = 192;
+constexpr int EPI_WARPS = 4;
+constexpr int SLOT = DMOE_SLOT_COLS;
+
+struct alignas(8) Ctrl {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t acc_full[ACC_BUFS];
+  uint64_t acc_empty[ACC_BUFS];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+  int bad;
+  int off[DMOE_MAX_EXPERTS + 1];         // expert row offsets
+  int mt[DMOE_MAX_EXPERTS + 1];          // exclusive prefix of m-tiles per expert
+};
+
+constexpr size_t kSmemBytes = 1024 + size_t(STAGES) * STAGE_BYTES + sizeof(Ctrl);
+
+struct KParams {
+  const int32_t* offsets;
+  int E, R, K, N, NT, KB;
+  uint16_t* out;
+  const uint16_t* grad_out;
+  const int32_t* row_src;
+  int topk;
+  float* slots;
+  float* dprob;
+  int* status;
+};
+
+// Shared-memory matrix descriptor for a K-major operand tile written by TMA
+// with 128-byte swizzling: rows of 128 bytes, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t smem_desc_k128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= uint64_t((saddr & 0x3FFFFu) >> 4);      // start address >> 4
+  d |= uint64_t(1) << 16;                       // leading byte offset (unused for swizzled K-major)
+  d |= uint64_t(1024 >> 4) << 32;               // stride byte offset: 8 rows x 128 B
+  d |= uint64_t(1) << 46;                       // descriptor version for tcgen05
+  d |= uint64_t(2) << 61;                       // swizzle mode: 128-byte
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 D, bf16 A and B, both K-major, M=128, N=256.
+constexpr uint32_t kIdesc = (1u << 4)                       // D format: f32
+                            | (1u << 7)                     // A format: bf16
+                            | (1u << 10)                    // B format: bf16
+                            | (uint32_t(BN >> 3) << 17)     // N >> 3
+                            | (uint32_t(BM >> 4) << 24);    // M >> 4
+
+struct Tile {
+  int e, row0, row_end, n0;
+};
+
+__device__ __forceinline__ Tile decode_tile(int t, const Ctrl& c, int E, int NT) {
+  // largest e in [0, E) with mt[e] * NT <= t  (skips empty experts)
+  int lo = 0, hi = E;
+  while (hi - lo > 1) {
+    int mid = (lo + hi) >> 1;
+    if (c.mt[mid] * NT <= t) lo = mid; else hi = mid;
+  }
+  int mtiles = c.mt[lo + 1] - c.mt[lo];
+  int local = t - c.mt[lo] * NT;
+  int n_tile = local / mtiles;
+  int m_tile = local - n_tile * mtiles;
+  Tile tl;
+  tl.e = lo;
+  tl.row0 = c.off[lo] + m_tile * BM;
+  tl.row_end = c.off[lo + 1];
+  tl.n0 = n_tile * BN;
+  return tl;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                    const KParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Ctrl& c = *reinterpret_cast<Ctrl*>(base + size_t(STAGES) * STAGE_BYTES);
+  const uint32_t stage0 = smem_u32(base);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int E = p.E;
+
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&c.full[s]), 1);
+      mbar_init(smem_u32(&c.empty[s]), 1);
+    }
+    for (int b = 0; b < ACC_BUFS; ++b) {
+      mbar_init(smem_u32(&c.acc_full[b]), 1);
+      mbar_init(smem_u32(&c.acc_empty[b]), EPI_WARPS);
+    }
+    mbar_init(smem_u32(&c.mma_done), 1);
+    c.abort = 0;
+    c.bad = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmap_a);
+    tma_prefetch_desc(&tmap_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&c.tmem_base), TMEM_COLS);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  // Expert offsets -> shared memory, validated, and the m-tile prefix.
+  for (int e = tid; e <= E; e += NUM_THREADS) c.off[e] = p.offsets[e];
+  __syncthreads();
+  int bad = 0;
+  for (int e = tid; e < E; e += NUM_THREADS) {
+    int a = c.off[e], b = c.off[e + 1];
+    if (b < a) bad = 1;
+    c.mt[e + 1] = (b > a) ? (b - a + BM - 1) / BM : 0;
+  }
+  if (tid == 0) {
+    if (c.off[0] != 0 || c.off[E] != p.R) bad = 1;
+    c.mt[0] = 0;
+  }
+  bad = __syncthreads_or(bad);
+  if (warp == 0) {
+    // inclusive scan of mt[1..E] in chunks of 32 (mt[0] = 0)
+    int carry = 0;
+    for (int b0 = 1; b0 <= E; b0 += 32) {
+      int i = b0 + lane;
+      int v = (i <= E) ? c.mt[i] : 0;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        int u = __shfl_up_sync(0xffffffffu, v, d);
+        if (lane >= d) v += u;
+      }
+      if (i <= E) c.mt[i] = v + carry;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (bad && tid == 0) record_error(p.status, DMOE_ERR_ROUTING);
+  const int total_tiles = bad ? 0 : c.mt[E] * p.NT;
+  const uint32_t tmem_base = c.tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer
+      int issued[STAGES];
+#pragma unroll
+      for (int s = 0; s < STAGES; ++s) issued[s] = 0;
+      int stage = 0;
+      uint32_t ph = 0;
+      for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+        const Tile tl = decode_tile(t, c, E, p.NT);
+        const int brow = tl.e * p.N + tl.n0;
+        bool ok = true;
+        for (int kb = 0; kb < p.KB; ++kb) {
+          if (!mbar_wait(smem_u32(&c.empty[stage]), ph ^ 1u, &c.abort, p.status)) { ok = false; break; }
+          const uint32_t full = smem_u32(&c.full[stage]);
+          const uint32_t sa = stage0 + stage * STAGE_BYTES;
+          mbar_arrive_expect_tx(full, STAGE_BYTES);
+          tma_load_2d(sa, &tmap_a, full, kb * BK, tl.row0);
+          tma_load_2d(sa + A_STAGE_BYTES, &tmap_b, full, kb * BK, brow);
+          ++issued[stage];
+          if (++stage == STAGES) { stage = 0; ph ^= 1u; }
+        }
+        if (!ok) break;
+      }
+      // let every copy this thread started land before the CTA can exit
+      for (int s = 0; s < STAGES; ++s)
+        if (issued[s] > 0) mbar_wait_drain(smem_u32(&c.full[s]), uint32_t(issued[s] - 1) & 1u);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------ MMA issuer
+      int stage = 0;
+      uint32_t ph = 0;
+      int acc = 0;
+      uint32_t aph = 0;
+      for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+        if (!mbar_wait(smem_u32(&c.acc_empty[acc]), aph ^ 1u, &c.abort, p.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
+        bool ok = true;
+        for (int kb = 0; kb < p.KB; ++kb) {
+          if (!mbar_wait(smem_u32(&c.full[stage]), ph, &c.abort, p.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = stage0 + stage * STAGE_BYTES;
+          const uint64_t adesc = smem_desc_k128(sa);
+          const uint64_t bdesc = smem_desc_k128(sa + A_STAGE_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+            // advance 32 bytes (16 bf16) along k inside the swizzled row
+            tc_mma_f16(d_tmem, adesc + uint64_t(kk * 2), bdesc + uint64_t(kk * 2), kIdesc,
+                       (kb | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit(smem_u32(&c.empty[stage]));
+          if (++stage == STAGES) { stage = 0; ph ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit(smem_u32(&c.acc_full[acc]));
+        if (++acc == ACC_BUFS) { acc = 0; aph ^= 1u; }
+      }
+      // every MMA must be finished before tensor memory is released
+      tc_commit(smem_u32(&c.mma_done));
+      mbar_wait_drain(smem_u32(&c.mma_done), 0);
+    }
+  } else {
+    // -------------------------------------------------- epilogue (4 warps)
+    const int q = warp & 3;               // TMEM lane quarter this warp may access
+    int acc = 0;
+    uint32_t aph = 0;
+    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+      const Tile tl = decode_tile(t, c, E, p.NT);
+      if (!mbar_wait(smem_u32(&c.acc_full[acc]), aph, &c.abort, p.status)) break;
+      tc_fence_after();
+      const int r = tl.row0 + q * 32 + lane;
+      int src = 0, tok = 0;
+      bool valid = r < tl.row_end;
+      if (MODE != int(GemmMode::kFwd) && valid) {
+        src = p.row_src[r];
+        if (unsigned(src) >= unsigned(p.R)) {   // corrupt row_src: report, never index with it
+          record_error(p.status, DMOE_ERR_ROUTING);
+          valid = false;
+        }
+        tok = src / p.topk;
+      }
+      const uint32_t tbase = tmem_base + uint32_t(acc * BN) + (uint32_t(q * 32) << 16);
+#pragma unroll 1
+      for (int h = 0; h < BN / SLOT; ++h) {
+        const int col0 = tl.n0 + h * SLOT;
+        if (col0 >= p.N) break;
+        float a[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) a[j] = 0.0f;
+#pragma unroll
+        for (int ch = 0; ch < SLOT / 32; ++ch) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tbase + uint32_t(h * SLOT + ch * 32), v);
+          tmem_wait_ld();
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2_rn(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+          if (valid) {
+            uint16_t* dst = p.out + size_t(r) * p.N + col0 + ch * 32;
+#pragma unroll
+            for (int vv = 0; vv < 4; ++vv)
+              stg_v4(dst + vv * 8, make_uint4(pk[4 * vv], pk[4 * vv + 1], pk[4 * vv + 2], pk[4 * vv + 3]));
+            if (MODE != int(GemmMode::kFwd)) {
+              const uint16_t* g = p.grad_out + size_t(tok) * p.N + col0 + ch * 32;
+#pragma unroll
+              for (int vv = 0; vv < 4; ++vv) {
+                const uint4 gv = ldg_nc_v4(g + vv * 8);
+                slot_accumulate8(a, gv, make_uint4(pk[4 * vv], pk[4 * vv + 1], pk[4 * vv + 2], pk[4 * vv + 3]));
+              }
+            }
+          }
+        }
+        if (MODE != int(GemmMode::kFwd) && valid) {
+          const float part = slot_tree(a);
+          const int s = col0 / SLOT;
+          if (MODE == int(GemmMode::kSlots))
+            p.slots[size_t(s) * p.R + r] = part;
+          else
+            atomicAdd(p.dprob + src, part);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&c.acc_empty[acc]));
+      if (++acc == ACC_BUFS) { acc = 0; aph ^= 1u; }
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor [rows, cols] (cols contiguous), box [box_rows, 64], 128-byte swizzle.
+bool make_tmap(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {uint32_t(BK), box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int MODE>
+cudaError_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const KParams& kp, int grid,
+                        cudaStream_t stream) {
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  grouped_gemm_kernel<MODE><<<grid, NUM_THREADS, kSmemBytes, stream>>>(ta, tb, kp);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_gemm(GemmMode mode, const GemmArgs& a, cudaStream_t stream) {
+  if (a.R == 0) return cudaSuccess;
+  CUtensorMap ta, tb;
+  if (!make_tmap(&ta, a.X, uint64_t(a.R), uint64_t(a.K), BM)) return cudaErrorInvalidValue;
+  if (!make_tmap(&tb, a.W, uint64_t(a.E) * a.N, uint64_t(a.K), BN)) return cudaErrorInvalidValue;
+  KParams kp;
+  kp.offsets = a.offsets;
+  kp.E = a.E;
+  kp.R = a.R;
+  kp.K = a.K;
+  kp.N = a.N;
+  kp.NT = (a.N + BN - 1) / BN;
+  kp.KB = (a.K + BK - 1) / BK;
+  kp.out = static_cast<uint16_t*>(a.out);
+  kp.grad_out = static_cast<const uint16_t*>(a.grad_out);
+  kp.row_src = a.row_src;
+  kp.topk = a.topk;
+  kp.slots = a.slots;
+  kp.dprob = a.dprob;
+  kp.status = a.status;
+  int grid = a.num_ctas > 0 ? a.num_ctas : device_sm_count();
+  switch (mode) {
+    case GemmMode::kFwd: return launch_mode<int(GemmMode::kFwd)>(ta, tb, kp, grid, stream);
+    case GemmMode::kSlots: return launch_mode<int(GemmMode::kSlots)>(ta, tb, kp, grid, stream);
+    case GemmMode::kAtomic: return launch_mode<int(GemmMode::kAtomic)>(ta, tb, kp, grid, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace dmoe

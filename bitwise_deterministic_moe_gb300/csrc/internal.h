@@ -1,0 +1,49 @@
+// Host-side launchers shared between the kernel translation units and the
+// C-ABI layer (api.cu).  All pointers are device pointers; validation of
+// user arguments happens in api.cu before any launcher is called.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace dmoe {
+
+enum class GemmMode : int { kFwd = 0, kSlots = 1, kAtomic = 2 };
+
+struct GemmArgs {
+  const void* X;              // bf16 [R, K]
+  const void* W;              // bf16 [E, N, K]
+  const int32_t* offsets;     // [E+1]
+  int R, E, K, N;
+  void* out;                  // bf16 [R, N]
+  const void* grad_out;       // bf16 [T, N]   (slots / atomic)
+  const int32_t* row_src;     // [R]           (slots / atomic)
+  int topk;
+  float* slots;               // [S, R]        (slots)
+  float* dprob;               // [T*topk]      (atomic)
+  int* status;                // device status word
+  int num_ctas;               // 0 = one per SM
+};
+
+cudaError_t launch_grouped_gemm(GemmMode mode, const GemmArgs& a, cudaStream_t stream);
+
+// routing
+size_t routing_scratch_bytes(long long R, int E);
+cudaError_t launch_permute(const int32_t* topk_ids, long long R, int E, int32_t* offsets, int32_t* row_src,
+                           void* scratch, int* status, cudaStream_t stream);
+
+// dprob (unfused epilogue and fixed-order combine)
+cudaError_t launch_dprob_epilogue(const void* grad_out, const void* expert_out, const int32_t* offsets,
+                                  const int32_t* row_src, int R, int E, int topk, int N, float* slots,
+                                  int* status, cudaStream_t stream);
+cudaError_t launch_dprob_combine(const float* slots, const int32_t* row_src, int R, int S, float* dprob,
+                                 cudaStream_t stream);
+
+// fingerprint
+cudaError_t launch_fingerprint(const void* data, size_t nbytes, int elem_size, int xor_kind, size_t chunk_bytes,
+                               int mode, uint64_t* chunk_hash, cudaStream_t stream);
+
+int device_sm_count();
+
+}  // namespace dmoe

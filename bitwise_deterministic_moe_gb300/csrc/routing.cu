@@ -1,0 +1,149 @@
+// Deterministic routing indices: a stable counting sort of the R = T*topk
+// routed entries by expert id.
+//
+// Routing maps are order-sensitive data ("NVIDIA fait passer le déterminisme
+// bit à bit de Megatron Core à 2432 GPU ...", section "Méthodologie de
+// débogage du non-déterminisme"), so every position is derived from counts and
+// prefix sums, never from atomic position tickets:
+//   1. histogram: one warp per block of 1024 entries counts ids per expert
+//      (integer counts are order-independent);
+//   2. block scan: one warp per expert turns its per-block counts into
+//      exclusive prefixes (within-expert rank base of each block);
+//   3. expert scan: one CTA scans the per-expert totals into expert_offsets;
+//   4. scatter: one warp per block walks its entries in order, 32 at a time;
+//      entries with equal ids are ranked by lane (match.any) and a per-expert
+//      running counter advances chunk by chunk, which keeps the sort stable.
+// Scratch: counts int32 [E][nblk] and totals int32 [E].
+#include "common.cuh"
+#include "internal.h"
+
+namespace dmoe {
+namespace {
+
+constexpr int kEntriesPerBlock = 1024;
+
+__global__ void __launch_bounds__(32)
+hist_kernel(const int32_t* __restrict__ ids, long long R, int E, int nblk, int32_t* __restrict__ counts,
+            int* status) {
+  __shared__ int cnt[DMOE_MAX_EXPERTS];
+  const int lane = threadIdx.x;
+  const int b = blockIdx.x;
+  for (int e = lane; e < E; e += 32) cnt[e] = 0;
+  __syncwarp();
+  const long long i0 = (long long)b * kEntriesPerBlock;
+  for (int k = lane; k < kEntriesPerBlock; k += 32) {
+    long long i = i0 + k;
+    if (i >= R) break;
+    int e = ids[i];
+    if (e < 0 || e >= E) {
+      record_error(status, DMOE_ERR_ROUTING);
+      continue;
+    }
+    atomicAdd(&cnt[e], 1);
+  }
+  __syncwarp();
+  for (int e = lane; e < E; e += 32) counts[(size_t)e * nblk + b] = cnt[e];
+}
+
+// One warp per expert: exclusive prefix over that expert's per-block counts.
+__global__ void __launch_bounds__(256)
+block_scan_kernel(int32_t* __restrict__ counts, int E, int nblk, int32_t* __restrict__ totals) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= E) return;
+  int32_t* row = counts + (size_t)warp * nblk;
+  int carry = 0;
+  for (int b0 = 0; b0 < nblk; b0 += 32) {
+    int i = b0 + lane;
+    int v = (i < nblk) ? row[i] : 0;
+    int x = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      int u = __shfl_up_sync(0xffffffffu, x, d);
+      if (lane >= d) x += u;
+    }
+    if (i < nblk) row[i] = carry + x - v;
+    carry += __shfl_sync(0xffffffffu, x, 31);
+  }
+  if (lane == 0) totals[warp] = carry;
+}
+
+// Single CTA of 1024 threads: offsets[0..E] = exclusive scan of totals.
+__global__ void __launch_bounds__(1024)
+expert_scan_kernel(const int32_t* __restrict__ totals, int E, int32_t* __restrict__ offsets) {
+  __shared__ int wsum[32];
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  int v = (tid < E) ? totals[tid] : 0;
+  int x = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    int u = __shfl_up_sync(0xffffffffu, x, d);
+    if (lane >= d) x += u;
+  }
+  if (lane == 31) wsum[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = wsum[lane];
+    int y = w;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      int u = __shfl_up_sync(0xffffffffu, y, d);
+      if (lane >= d) y += u;
+    }
+    wsum[lane] = y - w;  // exclusive prefix of warp sums
+  }
+  __syncthreads();
+  const int incl = x + wsum[warp];
+  if (tid < E) offsets[tid] = incl - v;
+  if (tid == E - 1) offsets[E] = incl;
+}
+
+__global__ void __launch_bounds__(32)
+scatter_kernel(const int32_t* __restrict__ ids, long long R, int E, int nblk, const int32_t* __restrict__ counts,
+               const int32_t* __restrict__ offsets, int32_t* __restrict__ row_src) {
+  __shared__ int next[DMOE_MAX_EXPERTS];
+  const int lane = threadIdx.x;
+  const int b = blockIdx.x;
+  for (int e = lane; e < E; e += 32) next[e] = offsets[e] + counts[(size_t)e * nblk + b];
+  __syncwarp();
+  const unsigned lt = (1u << lane) - 1u;
+  const long long i0 = (long long)b * kEntriesPerBlock;
+  for (int k0 = 0; k0 < kEntriesPerBlock; k0 += 32) {
+    const long long i = i0 + k0 + lane;
+    int e = (i < R) ? ids[i] : -1;
+    const bool ok = e >= 0 && e < E;
+    if (!ok) e = -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & lt);
+    int base = ok ? next[e] : 0;
+    __syncwarp();
+    if (ok) {
+      row_src[base + rank] = (int32_t)i;
+      if (rank == 0) next[e] = base + __popc(peers);
+    }
+    __syncwarp();
+  }
+}
+
+}  // namespace
+
+size_t routing_scratch_bytes(long long R, int E) {
+  long long nblk = (R + kEntriesPerBlock - 1) / kEntriesPerBlock;
+  size_t b = size_t(E) * size_t(nblk) * 4 + size_t(E) * 4;
+  return (b + 255) & ~size_t(255);
+}
+
+cudaError_t launch_permute(const int32_t* topk_ids, long long R, int E, int32_t* offsets, int32_t* row_src,
+                           void* scratch, int* status, cudaStream_t stream) {
+  const int nblk = int((R + kEntriesPerBlock - 1) / kEntriesPerBlock);
+  int32_t* counts = static_cast<int32_t*>(scratch);
+  int32_t* totals = counts + size_t(E) * nblk;
+  if (nblk > 0) hist_kernel<<<nblk, 32, 0, stream>>>(topk_ids, R, E, nblk, counts, status);
+  block_scan_kernel<<<(E * 32 + 255) / 256, 256, 0, stream>>>(counts, E, nblk, totals);
+  expert_scan_kernel<<<1, 1024, 0, stream>>>(totals, E, offsets);
+  if (nblk > 0) scatter_kernel<<<nblk, 32, 0, stream>>>(topk_ids, R, E, nblk, counts, offsets, row_src);
+  return cudaGetLastError();
+}
+
+}  // namespace dmoe

@@ -10,15 +10,18 @@ tech report: 550B 的 hybrid MoE 怎么训练、怎么 scale?" (concept list,
 the expert-imbalance figure in its "两次 divergence" table (MaxVio ~12 of a
 512/22 bound).  Everything is host numpy (PCG64), seed = 1234 + config index.
 
-Draw order per config (one Generator): routing, X_perm, W, grad_out, logits.
-Operands are N(0,1)/sqrt(K) drawn in float32 and rounded to bfloat16
-(round-to-nearest-even on the float32 bit pattern); bf16 tensors are returned
-as uint16 bit patterns.
+Routing and logits come from one sequential Generator (routing first).  The
+operands X_perm, W and grad_out are N(0,1)/sqrt(K) drawn in float32 from
+independently seeded blocks (so they can be filled by several threads) and
+rounded to bfloat16 (round-to-nearest-even on the float32 bit pattern); bf16
+tensors are returned as uint16 bit patterns.
 """
 from __future__ import annotations
 
+import concurrent.futures as cf
 import dataclasses
 import math
+import os
 
 import numpy as np
 
@@ -78,17 +81,33 @@ def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
     return (b.astype(np.uint32) << np.uint32(16)).view(np.float32)
 
 
-def _normal_bf16(rng: np.random.Generator, shape, scale: float, block: int = 1 << 24) -> np.ndarray:
-    """N(0,1)*scale in float32, rounded to bf16 bits; filled in blocks to bound memory."""
+_BLOCK = 1 << 22   # elements per independently seeded block
+
+
+def _normal_bf16(seed: int, tag: int, shape, scale: float) -> np.ndarray:
+    """N(0,1)*scale drawn in float32 and rounded to bf16 bits.
+
+    Block b of 2^22 elements is drawn from its own PCG64 stream seeded by
+    SeedSequence(seed, spawn_key=(tag, b)), so the bytes do not depend on how
+    many threads fill the blocks."""
     n = int(np.prod(shape))
     out = np.empty(n, dtype=np.uint16)
-    buf = np.empty(min(block, max(n, 1)), dtype=np.float32)
-    for s in range(0, n, block):
-        m = min(block, n - s)
-        v = buf[:m]
-        rng.standard_normal(out=v, dtype=np.float32)
+    nblocks = (n + _BLOCK - 1) // _BLOCK
+
+    def fill(b):
+        g = np.random.Generator(np.random.PCG64(np.random.SeedSequence(seed, spawn_key=(tag, b))))
+        m = min(_BLOCK, n - b * _BLOCK)
+        v = g.standard_normal(m, dtype=np.float32)
         v *= np.float32(scale)
-        out[s:s + m] = f32_to_bf16_bits(v)
+        out[b * _BLOCK:b * _BLOCK + m] = f32_to_bf16_bits(v)
+
+    workers = min(nblocks, max(1, len(os.sched_getaffinity(0)))) if nblocks else 1
+    if workers <= 1:
+        for b in range(nblocks):
+            fill(b)
+    else:
+        with cf.ThreadPoolExecutor(workers) as ex:
+            list(ex.map(fill, range(nblocks)))
     return out.reshape(shape)
 
 
@@ -169,9 +188,9 @@ def make_inputs(cfg: MoEConfig, with_weights: bool = True) -> MoEInputs:
     rng = np.random.default_rng(cfg.seed)
     ids = routing(cfg, rng)
     scale = 1.0 / math.sqrt(cfg.K)
-    X = _normal_bf16(rng, (cfg.R, cfg.K), scale)
-    W = _normal_bf16(rng, (cfg.E, cfg.N, cfg.K), scale) if with_weights else None
-    G = _normal_bf16(rng, (cfg.T, cfg.N), scale)
+    X = _normal_bf16(cfg.seed, 1, (cfg.R, cfg.K), scale)
+    W = _normal_bf16(cfg.seed, 2, (cfg.E, cfg.N, cfg.K), scale) if with_weights else None
+    G = _normal_bf16(cfg.seed, 3, (cfg.T, cfg.N), scale)
     logits = rng.standard_normal((cfg.T, cfg.topk), dtype=np.float32)
     z = np.exp(logits - logits.max(axis=1, keepdims=True))
     probs = (z / z.sum(axis=1, keepdims=True)).astype(np.float32)

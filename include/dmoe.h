@@ -1,0 +1,215 @@
+/*
+ * dmoe.h -- C ABI of libdmoe.so: a bitwise-deterministic MoE grouped GEMM with
+ * a fused routing-probability-gradient (dprob) epilogue, for GB300 (sm_103a).
+ *
+ * The operation (from "Trillion-Parameter Pretraining Goes Bitwise-
+ * Deterministic: NVIDIA Cuts the Determinism Tax to About 2%", section
+ * "Interpretation", and "NVIDIA fait passer le déterminisme bit à bit de
+ * Megatron Core à 2432 GPU avec seulement 2% de surcoût", section
+ * "Optimisation pour le Nemotron à mille milliards de paramètres"): in the
+ * grouped-GEMM epilogue several N-tiles contribute to the same dprob[token];
+ * accumulating them at one address makes the result depend on arrival order.
+ * Instead each N-tile writes a private slot and the slots are combined in a
+ * fixed order once all writers are done, so tiles still run in parallel and
+ * the result is identical run to run.
+ *
+ * Notation: T tokens, topk experts per token, E experts, R = T*topk permuted
+ * rows, K reduction (FFN intermediate) dim, N output (latent) dim, S =
+ * ceil(N/128) private slots per row.  Row r of the permuted layout came from
+ * the flat routing index row_src[r] = t*topk + j (token t, choice j).
+ *
+ * Conventions for every entry point:
+ *  - Every pointer is a DEVICE pointer unless marked "host".  All memory is
+ *    owned by the caller; the library never allocates or frees.
+ *  - Arrays are dense, row-major, contiguous.  bf16 arrays are passed as
+ *    void* holding IEEE bfloat16 values.  X_perm, W, expert_out and grad_out
+ *    must be 16-byte aligned (TMA and 16-byte vector access).
+ *  - Calls are asynchronous on `stream` (0 = legacy default stream).  The
+ *    return value reports host-side validation and launch errors only.
+ *    Errors found on the device (bad routing data, a wait that timed out)
+ *    are written to the status word at the start of the workspace `ws` and
+ *    read back with dmoe_read_status().
+ *  - Results are bitwise identical for any num_ctas >= 1, any stream, and
+ *    any number of concurrent calls on separate output buffers.
+ */
+#ifndef DMOE_H_
+#define DMOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* dmoe_stream_t;   /* a cudaStream_t */
+
+typedef enum dmoe_status {
+    DMOE_OK = 0,
+    DMOE_ERR_INVALID_ARG = 1,   /* null pointer, negative size, misalignment, R != T*topk */
+    DMOE_ERR_UNSUPPORTED = 2,   /* shape outside the supported range (see each call) */
+    DMOE_ERR_ROUTING = 3,       /* device: expert id outside [0,E) or offsets not a partition of [0,R) */
+    DMOE_ERR_TIMEOUT = 4,       /* device: a pipeline wait exceeded its limit; outputs are undefined */
+    DMOE_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed (launch, tensor-map encode) */
+    DMOE_ERR_WORKSPACE = 6      /* workspace missing or smaller than the *_workspace_bytes query */
+} dmoe_status;
+
+/* Element type codes recorded in fingerprint headers. */
+typedef enum dmoe_dtype {
+    DMOE_U8 = 0, DMOE_I8 = 1, DMOE_I16 = 2, DMOE_I32 = 3, DMOE_I64 = 4,
+    DMOE_F16 = 5, DMOE_BF16 = 6, DMOE_F32 = 7, DMOE_F64 = 8, DMOE_BOOL = 9,
+    DMOE_U16 = 10, DMOE_U32 = 11, DMOE_U64 = 12
+} dmoe_dtype;
+
+/* Launch options of the grouped GEMM.  num_ctas = persistent CTAs (0 = one
+ * per SM).  Any value gives the same bits. */
+typedef struct dmoe_launch {
+    int num_ctas;
+    int reserved;
+} dmoe_launch;
+
+/* Supported shapes of the grouped GEMM calls:
+ *   1 <= E <= DMOE_MAX_EXPERTS, 8 <= K <= 65536 with K % 8 == 0,
+ *   128 <= N <= 65536 with N % 128 == 0, 0 <= R < 2^31, E*N < 2^31. */
+#define DMOE_MAX_EXPERTS 1024
+#define DMOE_SLOT_COLS 128          /* columns per private dprob slot */
+#define DMOE_WS_STATUS_BYTES 256    /* status word region at the start of ws */
+
+const char* dmoe_status_string(int status);
+int dmoe_version(void);
+
+/* Workspace needed by every call below for a problem with T tokens, topk
+ * choices and E experts (routing scratch + the status word).  The caller
+ * allocates it once, ZERO-FILLED, and may reuse it for every call on that
+ * problem size; calls that share a workspace must be ordered on one stream. */
+size_t dmoe_workspace_bytes(int T, int topk, int E);
+
+/* Reads (synchronising `stream`) and clears the device status word in ws.
+ * Returns DMOE_OK or the first device-side error recorded since the last read. */
+dmoe_status dmoe_read_status(void* ws, dmoe_stream_t stream);
+
+/*
+ * Routing indices: a deterministic permutation of the R routed (token, choice)
+ * entries into expert-contiguous rows.  Routing maps are order-sensitive data
+ * ("NVIDIA fait passer ...", section "Méthodologie de débogage du
+ * non-déterminisme"), so the order is fixed: expert ascending, and within an
+ * expert the flat index t*topk+j ascending (a stable counting sort).
+ *   topk_ids        int32 [T, topk], ids in [0, E) (duplicates allowed)
+ *   expert_offsets  int32 [E+1] out: exclusive prefix of per-expert counts
+ *   row_src         int32 [R]   out: flat index of each permuted row
+ * Positions come from per-block counts and prefix sums, never from atomic
+ * position tickets.  An id outside [0,E) sets DMOE_ERR_ROUTING in ws; the
+ * outputs are then undefined.  T*topk may be 0.
+ */
+dmoe_status dmoe_permute_indices(const int32_t* topk_ids, int T, int topk, int E,
+                                 int32_t* expert_offsets, int32_t* row_src,
+                                 void* ws, size_t ws_bytes, dmoe_stream_t stream);
+
+/*
+ * Grouped GEMM (FFN-out projection into the latent dim): for every expert e
+ * and permuted row r in [off[e], off[e+1]):
+ *     expert_out[r, n] = bf16_rn( sum_c X_perm[r, c] * W[e, n, c] )
+ * fp32 accumulation on the tensor cores, one rounding to bf16 (nearest even).
+ *   X_perm          bf16 [R, K]       rows in expert-permuted order
+ *   W               bf16 [E, N, K]    per-expert weight, K contiguous
+ *   expert_offsets  int32 [E+1]       off[0] = 0, non-decreasing, off[E] = R
+ *   expert_out      bf16 [R, N]       out
+ * Offsets that are not a partition of [0,R) set DMOE_ERR_ROUTING and skip the
+ * GEMM.  ws: at least DMOE_WS_STATUS_BYTES bytes.
+ */
+dmoe_status moe_grouped_gemm_fwd(const void* X_perm, const void* W, const int32_t* expert_offsets,
+                                 int R, int E, int K, int N, void* expert_out,
+                                 const dmoe_launch* launch, void* ws, size_t ws_bytes,
+                                 dmoe_stream_t stream);
+
+/*
+ * Grouped GEMM with the fused private-slot dprob epilogue and the fixed-order
+ * combine (the deterministic path).  Besides expert_out as above:
+ *     slots[s, r] = sum over the 128 columns n of slot s of
+ *                   float(grad_out[t(r), n]) * float(expert_out[r, n])
+ * using the STORED bf16 expert_out value, summed in this fixed tree: eight
+ * fp32 partials a_j = sum_{i=0..15} p[8i+j] (i ascending, fused multiply-add
+ * from +0), then ((a0+a1)+(a2+a3))+((a4+a5)+(a6+a7)).  Each N-tile writes
+ * only its own slots.  Then, after all writers are done,
+ *     dprob[row_src[r]] = (((slots[0,r] + slots[1,r]) + slots[2,r]) + ...)
+ * in ascending slot order, fp32.
+ *   grad_out  bf16 [T, N]      gradient at the expert-combine output, by token
+ *   row_src   int32 [R]        from dmoe_permute_indices
+ *   slots     fp32 [S, R]      scratch owned by the caller (S = N/128)
+ *   dprob     fp32 [T, topk]   out
+ * R must equal T*topk.
+ */
+dmoe_status moe_grouped_gemm_dprob(const void* X_perm, const void* W, const int32_t* expert_offsets,
+                                   int R, int E, int K, int N, void* expert_out,
+                                   const void* grad_out, const int32_t* row_src, int T, int topk,
+                                   float* slots, float* dprob,
+                                   const dmoe_launch* launch, void* ws, size_t ws_bytes,
+                                   dmoe_stream_t stream);
+
+/*
+ * The nondeterministic control (the original form the pages describe): the
+ * same GEMM and per-slot partials, but every partial is added with an fp32
+ * atomicAdd into dprob[row_src[r]] after the call zero-fills dprob on
+ * `stream`.  The order of the additions depends on CTA scheduling, so the
+ * low bits of dprob may differ run to run.  Kept only to measure the
+ * determinism tax.
+ */
+dmoe_status moe_grouped_gemm_dprob_atomic(const void* X_perm, const void* W, const int32_t* expert_offsets,
+                                          int R, int E, int K, int N, void* expert_out,
+                                          const void* grad_out, const int32_t* row_src, int T, int topk,
+                                          float* dprob,
+                                          const dmoe_launch* launch, void* ws, size_t ws_bytes,
+                                          dmoe_stream_t stream);
+
+/*
+ * Unfused private-slot epilogue: the slot partials of moe_grouped_gemm_dprob
+ * computed from an expert_out already in memory, with the identical
+ * arithmetic, so the result is bitwise equal to the fused epilogue's slots.
+ *   grad_out bf16 [T,N], expert_out bf16 [R,N], expert_offsets int32 [E+1]
+ *   (rows r >= off[E] are skipped), row_src int32 [R], slots fp32 [S,R] out.
+ */
+dmoe_status moe_dprob_epilogue(const void* grad_out, const void* expert_out, const int32_t* expert_offsets,
+                               const int32_t* row_src, int R, int E, int T, int topk, int N,
+                               float* slots, dmoe_stream_t stream);
+
+/*
+ * Fixed-order slot combine: dprob[row_src[r]] = sum of slots[0..S-1, r],
+ * left to right in ascending s, fp32.  Bitwise equal to the combine inside
+ * moe_grouped_gemm_dprob.
+ *   slots fp32 [S, R], row_src int32 [R], dprob fp32 [T*topk] out (R == T*topk).
+ */
+dmoe_status moe_dprob_combine(const float* slots, const int32_t* row_src, int R, int S, int T, int topk,
+                              float* dprob, dmoe_stream_t stream);
+
+/*
+ * Chunk-wise tensor fingerprint ("NVIDIA fait passer ...", section "Méthodologie
+ * de débogage du non-déterminisme": fingerprints computed on the GPU, with
+ * shape, dtype and element count recorded, chunk-wise for order-sensitive
+ * data).  The bytes [0, nbytes) are cut into chunks of chunk_bytes (the last
+ * may be shorter) and each chunk c gets one 64-bit hash in chunk_hash[c]:
+ *   mode 0 (positional, raw bits): words w_i = little-endian uint32 at byte
+ *     4i (tail zero-padded), i the word index in the whole buffer;
+ *     acc = sum_i fmix32(w_i ^ (i * 0x9E3779B9 mod 2^32)) mod 2^64 over the chunk;
+ *     chunk_hash[c] = sm64(acc ^ (c << 32) ^ chunk_length_in_bytes),
+ *     fmix32 = MurmurHash3's finalizer, sm64 = splitmix64's output function.
+ *   mode 1 (xor): xor over the chunk's elements widened to 64 bits (floats to
+ *     binary64 bit patterns, signed ints sign-extended, unsigned zero-extended),
+ *     the reduction torch.hash_tensor applies to a whole tensor.  NaN
+ *     payloads are not specified.
+ * header_hash (HOST out) = sm64 chain over (dtype, ndim, shape[0..ndim-1],
+ *   numel, nbytes): h = sm64(dtype); h = sm64(h ^ v) for each v in order.
+ *   data       device, any alignment (16-byte alignment takes the fast path)
+ *   shape      HOST int64 [ndim]; nbytes must equal numel * element size
+ *   chunk_bytes  > 0, multiple of 16
+ *   chunk_hash uint64 [dmoe_fingerprint_num_chunks(nbytes, chunk_bytes)] out
+ */
+size_t dmoe_fingerprint_num_chunks(size_t nbytes, size_t chunk_bytes);
+dmoe_status dmoe_fingerprint(const void* data, size_t nbytes, int dtype, int ndim, const int64_t* shape,
+                             size_t chunk_bytes, int mode, uint64_t* chunk_hash, uint64_t* header_hash,
+                             dmoe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DMOE_H_ */

@@ -1,0 +1,118 @@
+"""Bitwise determinism: outputs are identical across repeated launches,
+persistent grid sizes and concurrent streams, proven by chunk fingerprints
+(1 MiB chunks) of expert_out, slots and dprob."""
+import numpy as np
+import pytest
+import torch
+
+from bitwise_deterministic_moe_gb300 import api, synth
+from tests import gpu_util
+from tests.gpu_util import Problem
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    gpu_util.ensure_built()
+
+
+def fps(*ts):
+    out = []
+    for t in ts:
+        ch, h = api.fingerprint(t)
+        out.append((ch.clone(), h))
+    return out
+
+
+def same(a, b):
+    return all(torch.equal(x[0], y[0]) and x[1] == y[1] for x, y in zip(a, b))
+
+
+def test_repeat_grids_streams_small():
+    cfg = synth.CONFIGS["small"]
+    prob = Problem(cfg)
+    out, dprob, slots = prob.run_dprob()
+    ref = fps(out, slots, dprob)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for grid in (sms, sms // 2, 37, 1):
+        for _ in range(3):
+            o, d, s = prob.run_dprob(num_ctas=grid)
+            assert same(fps(o, s, d), ref), grid
+    assert api.read_status(prob.ws) == 0
+
+
+def test_stress_100_launches_3_grids_2_streams():
+    cfg = synth.CONFIGS["stress"]
+    prob = Problem(cfg)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    out, dprob, slots = prob.run_dprob()
+    ref = fps(out, slots, dprob)
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    bufs = [prob.run_dprob() for _ in streams]          # separate outputs per stream
+    torch.cuda.synchronize()
+    mismatches = 0
+    launches = 0
+    for it in range(100 // 2):
+        for grid in (sms, sms // 2, 37):
+            for s, (o, d, sl) in zip(streams, bufs):
+                with torch.cuda.stream(s):
+                    prob.run_dprob(num_ctas=grid, out=o, slots=sl, dprob=d, stream=s)
+                launches += 1
+            if it % 10 == 0 or it == 100 // 2 - 1:
+                torch.cuda.synchronize()
+                for o, d, sl in bufs:
+                    mismatches += 0 if same(fps(o, sl, d), ref) else 1
+    torch.cuda.synchronize()
+    for o, d, sl in bufs:
+        mismatches += 0 if same(fps(o, sl, d), ref) else 1
+    assert launches == 300
+    assert mismatches == 0
+    assert api.read_status(prob.ws) == 0
+
+
+def test_atomic_control_differs_run_to_run_is_recorded():
+    """The control may differ between runs; the count is reported, not asserted."""
+    cfg = synth.CONFIGS["small"]
+    prob = Problem(cfg)
+    _, d0 = api.grouped_gemm_dprob_atomic(prob.X, prob.W, prob.off, prob.G, prob.src, cfg.topk, prob.ws)
+    diffs = []
+    for _ in range(5):
+        _, d1 = api.grouped_gemm_dprob_atomic(prob.X, prob.W, prob.off, prob.G, prob.src, cfg.topk, prob.ws)
+        diffs.append(int((d0.view(torch.int32) != d1.view(torch.int32)).sum().item()))
+    print("atomic control: differing dprob elements per rerun:", diffs)
+
+
+def test_relabel_and_token_permutation_bitwise():
+    """Relabelling experts (W'[pi(e)] = W[e]) and permuting tokens leaves every
+    dprob and expert_out row bitwise unchanged on the GPU."""
+    cfg = synth.custom_config("perm", T=2000, E=48, topk=4, K=256, N=512, index=401)
+    inp = synth.make_inputs(cfg)
+    import oracle
+    off, src = oracle.routing(inp.topk_ids, cfg.E)
+    inv = np.empty(cfg.R, np.int64)
+    inv[src] = np.arange(cfg.R)
+    X_tok = inp.X[inv].reshape(cfg.T, cfg.topk, cfg.K)
+    base = Problem(cfg, inp)
+    out0, d0, _ = base.run_dprob()
+    rng = np.random.default_rng(2)
+    pi = rng.permutation(cfg.E)
+    W2 = np.empty_like(inp.W)
+    W2[pi] = inp.W
+    ids2 = pi[inp.topk_ids].astype(np.int32)
+    tp = rng.permutation(cfg.T)
+    ids2 = ids2[tp]
+    off2, src2 = oracle.routing(ids2, cfg.E)
+    X2 = X_tok[tp].reshape(cfg.R, cfg.K)[src2]
+    p2 = Problem(cfg, synth.MoEInputs(cfg, ids2, X2, W2, inp.G[tp], inp.probs[tp]))
+    out2, d2, _ = p2.run_dprob()
+    tpt = torch.from_numpy(tp).cuda()
+    assert torch.equal(d2.view(torch.int32), d0.view(torch.int32)[tpt])
+    # expert_out rows: row of (t, j) in each layout
+    flat0 = torch.from_numpy(inv).cuda()                     # (t*k+j) -> row in base
+    inv2 = np.empty(cfg.R, np.int64)
+    inv2[src2] = np.arange(cfg.R)
+    tj2 = (tp[:, None] * cfg.topk + np.arange(cfg.topk)[None, :]).reshape(-1)   # base flat index of new (t, j)
+    rows_base = flat0[torch.from_numpy(tj2).cuda()]
+    rows_new = torch.from_numpy(inv2).cuda()
+    assert torch.equal(out2.view(torch.int16)[rows_new], out0.view(torch.int16)[rows_base])

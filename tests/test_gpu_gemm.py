@@ -1,0 +1,129 @@
+"""Grouped GEMM + private-slot dprob on the GPU vs the oracle, element by
+element, on shapes that span several tiles, ragged expert tails, empty
+experts, K tails and half-width N tiles; plus sampled rows at the full
+LatentMoE-shaped size in the benchmark's launch configuration."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from bitwise_deterministic_moe_gb300 import api, synth
+from tests import gpu_util
+from tests.gpu_util import Problem
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    gpu_util.ensure_built()
+
+
+SHAPES = [
+    synth.CONFIGS["tiny"],
+    synth.custom_config("ragged", T=600, E=12, topk=3, K=320, N=384, index=301),   # K tail, N % 256 == 128
+    synth.custom_config("wide", T=300, E=5, topk=2, K=72, N=1024, index=302),      # K < one stage
+    synth.custom_config("manyexp", T=700, E=1024, topk=8, K=128, N=256, index=303),  # many small experts
+    synth.custom_config("zipf", T=1024, E=64, topk=6, K=256, N=512, routing="zipf", index=304),
+]
+
+
+@pytest.mark.parametrize("cfg", SHAPES, ids=[c.name for c in SHAPES])
+def test_full_parity_small_shapes(cfg):
+    prob = Problem(cfg)
+    out, dprob, slots = prob.run_dprob()
+    assert api.read_status(prob.ws) == 0
+    rows = np.arange(cfg.R)
+    gpu_util.check_rows_against_oracle(prob, out, slots, dprob, rows)
+
+
+@pytest.mark.parametrize("cfg", SHAPES[:2], ids=[c.name for c in SHAPES[:2]])
+def test_fwd_equals_dprob_output_and_unfused_epilogue(cfg):
+    prob = Problem(cfg)
+    out, dprob, slots = prob.run_dprob()
+    out2 = api.grouped_gemm_fwd(prob.X, prob.W, prob.off, prob.ws)
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    slots2 = api.dprob_epilogue(prob.G, out, prob.off, prob.src, cfg.topk)
+    assert torch.equal(slots.view(torch.int32), slots2.view(torch.int32))      # fused == unfused, bitwise
+    dprob2 = api.dprob_combine(slots2, prob.src, cfg.topk)
+    assert torch.equal(dprob.view(torch.int32), dprob2.view(torch.int32))
+
+
+def test_unfused_epilogue_on_oracle_output():
+    """The unfused epilogue + combine on the ORACLE's bf16 output vs oracle dots."""
+    cfg = SHAPES[1]
+    inp = synth.make_inputs(cfg)
+    ref = oracle.full(inp)
+    ws = api.workspace(cfg.T, cfg.topk, cfg.E)
+    off = torch.from_numpy(ref["off"]).cuda()
+    src = torch.from_numpy(ref["row_src"]).cuda()
+    Yb = gpu_util.bf16_dev(ref["Yb"])
+    G = gpu_util.bf16_dev(inp.G)
+    slots = api.dprob_epilogue(G, Yb, off, src, cfg.topk)
+    dprob = api.dprob_combine(slots, src, cfg.topk)
+    P = ref["P"]
+    got_p = slots.t().double().cpu().numpy()
+    assert np.abs(got_p - P).max() <= 2e-3 * np.abs(P).max()
+    D = ref["dprob"]
+    assert np.abs(dprob.double().cpu().numpy() - D).max() <= 2e-3 * np.abs(D).max()
+
+
+def test_atomic_control_close_to_deterministic():
+    cfg = SHAPES[4]
+    prob = Problem(cfg)
+    out, dprob, _ = prob.run_dprob()
+    out_a, dprob_a = api.grouped_gemm_dprob_atomic(prob.X, prob.W, prob.off, prob.G, prob.src, cfg.topk, prob.ws)
+    assert torch.equal(out.view(torch.int16), out_a.view(torch.int16))
+    scale = dprob.abs().max().item()
+    assert (dprob - dprob_a).abs().max().item() <= 1e-5 * scale
+    rows = np.arange(0, cfg.R, 7)
+    gpu_util.check_rows_against_oracle(prob, out_a, None, dprob_a, rows)
+
+
+def test_empty_experts_and_hot_expert():
+    cfg = synth.custom_config("holes", T=900, E=40, topk=4, K=192, N=256, index=305)
+    inp = synth.make_inputs(cfg)
+    ids = inp.topk_ids.copy()
+    ids[ids % 5 == 0] = 1           # experts 0,5,10,... empty; expert 1 hot (duplicates allowed)
+    inp2 = synth.MoEInputs(cfg, ids, inp.X, inp.W, inp.G, inp.probs)
+    prob = Problem(cfg, inp2)
+    out, dprob, slots = prob.run_dprob()
+    assert api.read_status(prob.ws) == 0
+    gpu_util.check_rows_against_oracle(prob, out, slots, dprob, np.arange(cfg.R))
+
+
+def test_bad_offsets_set_routing_status():
+    cfg = SHAPES[0]
+    prob = Problem(cfg)
+    bad = prob.off.clone()
+    bad[3] = bad[4] + 1            # not monotone
+    api.grouped_gemm_fwd(prob.X, prob.W, bad, prob.ws)
+    assert api.read_status(prob.ws) == 3
+    bad = prob.off.clone()
+    bad[-1] -= 1                   # does not end at R
+    api.grouped_gemm_fwd(prob.X, prob.W, bad, prob.ws)
+    assert api.read_status(prob.ws) == 3
+    assert api.read_status(prob.ws) == 0   # cleared by the read
+
+
+def test_zero_rows():
+    ws = api.workspace(0, 2, 4)
+    X = torch.empty(0, 64, dtype=torch.bfloat16, device="cuda")
+    W = torch.randn(4, 256, 64, device="cuda").to(torch.bfloat16)
+    off = torch.zeros(5, dtype=torch.int32, device="cuda")
+    out = api.grouped_gemm_fwd(X, W, off, ws)
+    torch.cuda.synchronize()
+    assert out.shape == (0, 256)
+
+
+@pytest.mark.parametrize("name", ["small", "latent"])
+def test_full_size_sampled_rows(name):
+    """The benchmark's configuration (one CTA per SM) at full size, on sampled
+    rows the oracle computes one by one."""
+    cfg = synth.CONFIGS[name]
+    prob = Problem(cfg)
+    out, dprob, slots = prob.run_dprob()
+    assert api.read_status(prob.ws) == 0
+    off = prob.off.cpu().numpy()
+    rows = gpu_util.sample_rows(off, 96, seed=cfg.seed)
+    gpu_util.check_rows_against_oracle(prob, out, slots, dprob, rows)

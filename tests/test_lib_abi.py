@@ -1,0 +1,103 @@
+"""The C-ABI library builds for sm_103a, loads, and exports every entry point
+include/dmoe.h declares.  Host-side argument validation is exercised with
+calls that are rejected before any CUDA call is made (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from bitwise_deterministic_moe_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dmoe.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^[A-Za-z_][\w\s\*]*?\b((?:dmoe|moe)_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for want in ["moe_grouped_gemm_fwd", "moe_grouped_gemm_dprob", "moe_grouped_gemm_dprob_atomic",
+                 "moe_dprob_epilogue", "moe_dprob_combine", "dmoe_permute_indices", "dmoe_fingerprint",
+                 "dmoe_read_status", "dmoe_workspace_bytes"]:
+        assert want in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings_and_sizes(lib):
+    lib.dmoe_status_string.restype = ctypes.c_char_p
+    assert lib.dmoe_status_string(0) == b"ok"
+    assert b"routing" in lib.dmoe_status_string(3)
+    lib.dmoe_workspace_bytes.restype = ctypes.c_size_t
+    # status region + per-expert counts of ceil(R/1024) blocks + totals, rounded to 256
+    assert lib.dmoe_workspace_bytes(8192, 22, 512) == 256 + ((512 * 176 * 4 + 512 * 4 + 255) // 256) * 256
+    assert lib.dmoe_workspace_bytes(0, 4, 8) == 256 + 256
+    lib.dmoe_fingerprint_num_chunks.restype = ctypes.c_size_t
+    lib.dmoe_fingerprint_num_chunks.argtypes = [ctypes.c_size_t, ctypes.c_size_t]
+    assert lib.dmoe_fingerprint_num_chunks(0, 1 << 20) == 0
+    assert lib.dmoe_fingerprint_num_chunks((1 << 20) + 1, 1 << 20) == 2
+
+
+def test_invalid_arguments_rejected_on_host(lib):
+    P, I, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    f = lib.moe_grouped_gemm_fwd
+    f.argtypes = [P, P, P, I, I, I, I, P, P, P, SZ, P]
+    f.restype = I
+    # null operands -> DMOE_ERR_INVALID_ARG (1)
+    assert f(None, None, None, 16, 2, 64, 256, None, None, None, 0, None) == 1
+    # misaligned pointers -> invalid argument
+    assert f(8, 16, 16, 16, 2, 64, 256, 16, None, 16, 4096, None) == 1
+    # N not a multiple of 128 -> DMOE_ERR_UNSUPPORTED (2); too many experts too
+    assert f(16, 16, 16, 16, 2, 64, 200, 16, None, 16, 4096, None) == 2
+    assert f(16, 16, 16, 16, 2000, 64, 256, 16, None, 16, 4096, None) == 2
+    # K not a multiple of 8 -> unsupported
+    assert f(16, 16, 16, 16, 2, 60, 256, 16, None, 16, 4096, None) == 2
+    # missing workspace -> DMOE_ERR_WORKSPACE (6)
+    assert f(16, 16, 16, 16, 2, 64, 256, 16, None, None, 0, None) == 6
+    g = lib.moe_grouped_gemm_dprob
+    g.argtypes = [P, P, P, I, I, I, I, P, P, P, I, I, P, P, P, P, SZ, P]
+    g.restype = I
+    # R != T * topk -> invalid argument
+    assert g(16, 16, 16, 10, 2, 64, 256, 16, 16, 16, 3, 4, 16, 16, None, 16, 4096, None) == 1
+    p = lib.dmoe_permute_indices
+    p.argtypes = [P, I, I, I, P, P, P, SZ, P]
+    p.restype = I
+    assert p(16, 4, 2, 0, 16, 16, 16, 4096, None) == 1          # E = 0
+    assert p(16, 4, 2, 4096, 16, 16, 16, 4096, None) == 2       # E > 1024
+    assert p(16, 4, 2, 8, 16, 16, 16, 8, None) == 6             # workspace too small
+    fp = lib.dmoe_fingerprint
+    fp.argtypes = [P, SZ, I, I, ctypes.POINTER(ctypes.c_int64), SZ, I, P, ctypes.POINTER(ctypes.c_uint64), P]
+    fp.restype = I
+    shape = (ctypes.c_int64 * 1)(10)
+    h = ctypes.c_uint64()
+    assert fp(16, 10, 0, 1, shape, 100, 0, 16, ctypes.byref(h), None) == 1   # chunk not a multiple of 16
+    assert fp(16, 11, 0, 1, shape, 64, 0, 16, ctypes.byref(h), None) == 1    # nbytes != numel * size
+
+
+def test_header_hash_matches_oracle_without_gpu(lib):
+    """An empty tensor makes no device call, so its header can be checked here."""
+    import oracle
+    P, I, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    fp = lib.dmoe_fingerprint
+    fp.argtypes = [P, SZ, I, I, ctypes.POINTER(ctypes.c_int64), SZ, I, P, ctypes.POINTER(ctypes.c_uint64), P]
+    fp.restype = I
+    for code, shape in [(6, (0, 4)), (7, (3, 0, 5)), (0, (0,))]:
+        arr = (ctypes.c_int64 * len(shape))(*shape)
+        h = ctypes.c_uint64()
+        assert fp(None, 0, code, len(shape), arr, 1 << 20, 0, None, ctypes.byref(h), None) == 0
+        assert h.value == oracle.header_hash(code, shape)
