@@ -70,8 +70,9 @@ int* status_ptr(void* ws) { return static_cast<int*>(ws); }
 
 dmoe_status check_gemm_shape(const void* X, const void* W, const int32_t* off, int R, int E, int K, int N,
                              const void* out, void* ws, size_t ws_bytes) {
-  if (!X || !W || !off || !out) return DMOE_ERR_INVALID_ARG;
+  if (!W || !off) return DMOE_ERR_INVALID_ARG;
   if (R < 0 || E < 1 || K < 1 || N < 1) return DMOE_ERR_INVALID_ARG;
+  if (R > 0 && (!X || !out)) return DMOE_ERR_INVALID_ARG;   // X_perm / expert_out may be null when R == 0
   if (!aligned16(X) || !aligned16(W) || !aligned16(out)) return DMOE_ERR_INVALID_ARG;
   if (E > DMOE_MAX_EXPERTS || K % 8 != 0 || K > 65536 || N % DMOE_SLOT_COLS != 0 || N > 65536)
     return DMOE_ERR_UNSUPPORTED;
