@@ -20,7 +20,8 @@
  *
  * Conventions for every entry point:
  *  - Every pointer is a DEVICE pointer unless marked "host".  All memory is
- *    owned by the caller; the library never allocates or frees.
+ *    owned by the caller; the library never allocates or frees.  (The one
+ *    exception is the fixed scratch array of moe_grouped_gemm_dprob_noalloc.)
  *  - Arrays are dense, row-major, contiguous.  bf16 arrays are passed as
  *    void* holding IEEE bfloat16 values.  X_perm, W, expert_out and grad_out
  *    must be 16-byte aligned (TMA and 16-byte vector access).
@@ -160,6 +161,36 @@ dmoe_status moe_grouped_gemm_dprob_atomic(const void* X_perm, const void* W, con
                                           float* dprob,
                                           const dmoe_launch* launch, void* ws, size_t ws_bytes,
                                           dmoe_stream_t stream);
+
+/*
+ * No-allocation variant of moe_grouped_gemm_dprob.  The pages have no
+ * counterpart; it exists for callers that cannot allocate device memory:
+ * code hosted by another runtime that only hands it input and output buffers
+ * (a plugin or custom-op interface with no allocation hook, an engine whose
+ * memory is partitioned in advance) and latency-critical loops that must not
+ * call cudaMalloc, which can synchronise the device.
+ *
+ * Same inputs, outputs and bits as moe_grouped_gemm_dprob, but the [S, R]
+ * slot scratch lives in a fixed-size device array owned by the library
+ * (DMOE_NOALLOC_MAX_SLOT_VALUES fp32 values = 16 MiB, held on every GPU that
+ * loads the library until the process exits), and no workspace is taken.
+ *  - S * R > DMOE_NOALLOC_MAX_SLOT_VALUES returns DMOE_ERR_UNSUPPORTED.
+ *  - Allocates nothing: no cudaMalloc/cudaFree, no allocating library call.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture.
+ *  - All calls share the one array and it keeps the last call's contents
+ *    (nothing in it needs to start at zero); calls whose work overlaps on
+ *    the GPU (other streams, other threads) race on it.
+ *  - Device-side errors (bad routing data, a timed-out wait) are not
+ *    recorded; outputs are then undefined.  Use moe_grouped_gemm_dprob with a
+ *    workspace to have them reported.
+ */
+#define DMOE_NOALLOC_MAX_SLOT_VALUES 4194304
+dmoe_status moe_grouped_gemm_dprob_noalloc(const void* X_perm, const void* W, const int32_t* expert_offsets,
+                                           int R, int E, int K, int N, void* expert_out,
+                                           const void* grad_out, const int32_t* row_src, int T, int topk,
+                                           float* dprob, const dmoe_launch* launch, dmoe_stream_t stream);
 
 /*
  * Unfused private-slot epilogue: the slot partials of moe_grouped_gemm_dprob
