@@ -195,15 +195,22 @@ __device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
   return r;
 }
 
-// The fixed in-slot reduction shared by the fused and unfused epilogues:
-// eight fp32 partials acc[j] (= sum over i of p[8i+j], i ascending) folded
-// as ((a0+a1)+(a2+a3))+((a4+a5)+(a6+a7)).
+// The fixed in-slot reduction shared by the fused and unfused epilogues.
+// A 128-column slot is 16 groups of 8 columns; group g belongs to part
+// k = g % 4.  Part k keeps eight fp32 partials acc[j] = sum over its groups
+// g = k, k+4, k+8, k+12 (ascending) of p[8g+j], fused multiply-add from +0,
+// folds them with slot_tree, and the four parts are combined as
+// (L0 + L1) + (L2 + L3).
 __device__ __forceinline__ float slot_tree(const float (&a)[8]) {
   float s01 = __fadd_rn(a[0], a[1]);
   float s23 = __fadd_rn(a[2], a[3]);
   float s45 = __fadd_rn(a[4], a[5]);
   float s67 = __fadd_rn(a[6], a[7]);
   return __fadd_rn(__fadd_rn(s01, s23), __fadd_rn(s45, s67));
+}
+
+__device__ __forceinline__ float slot_parts(float l0, float l1, float l2, float l3) {
+  return __fadd_rn(__fadd_rn(l0, l1), __fadd_rn(l2, l3));
 }
 
 // Accumulate one 16-byte group (8 consecutive columns) of a slot:
@@ -224,6 +231,18 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
   asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void sts_v4(uint32_t addr, const uint4& v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+               : "memory");
   return v;
 }
 

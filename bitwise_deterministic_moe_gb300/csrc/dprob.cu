@@ -33,16 +33,21 @@ dprob_epilogue_kernel(const uint16_t* __restrict__ grad_out, const uint16_t* __r
   const int tok = src / topk;
   const uint16_t* g = grad_out + size_t(tok) * N + size_t(s) * SLOT;
   const uint16_t* y = expert_out + size_t(r) * N + size_t(s) * SLOT;
-  float a[8];
+  float part[4];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) a[j] = 0.0f;
-#pragma unroll 4
-  for (int i = 0; i < SLOT / 8; ++i) {
-    const uint4 gv = ldg_nc_v4(g + i * 8);
-    const uint4 yv = ldg_nc_v4(y + i * 8);
-    slot_accumulate8(a, gv, yv);
+  for (int k = 0; k < 4; ++k) {
+    float a[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) a[j] = 0.0f;
+#pragma unroll
+    for (int gi = k; gi < SLOT / 8; gi += 4) {
+      const uint4 gv = ldg_nc_v4(g + gi * 8);
+      const uint4 yv = ldg_nc_v4(y + gi * 8);
+      slot_accumulate8(a, gv, yv);
+    }
+    part[k] = slot_tree(a);
   }
-  slots[size_t(s) * R + r] = slot_tree(a);
+  slots[size_t(s) * R + r] = slot_parts(part[0], part[1], part[2], part[3]);
 }
 
 // One thread per permuted row: ascending-slot fp32 sum, scattered to dprob.

@@ -10,14 +10,16 @@
 // output columns, independent of the MMA tile width, so the bits do not
 // depend on the tile shape either.
 //
-// Design (one CTA per SM, persistent, warp-specialised, 192 threads):
+// Design (one CTA per SM, persistent, warp-specialised, 320 threads):
 //   warp 0  TMA producer: A tile [128 rows x 64 k] and B tile [256 n x 64 k]
 //           per stage, 128-byte swizzle, 4-stage ring in shared memory.
 //   warp 1  tcgen05.mma issuer (one thread): 128x256x16 bf16 MMAs, fp32
 //           accumulators in tensor memory, double-buffered (2 x 256 columns).
-//   warps 2-5  epilogue: tcgen05.ld of the accumulator, bf16 rounding, masked
+//   warps 2-9  epilogue: tcgen05.ld of the accumulator, bf16 rounding, masked
 //           stores of expert_out rows, and the per-slot dot products with
-//           grad_out in the fixed tree (one thread per output row).
+//           grad_out in the fixed tree (one thread per output row; one warp
+//           per 32 rows x 128 columns = one private slot).  The row's
+//           grad_out slice is fetched before the accumulator is ready.
 // Tiles are enumerated expert-major, then n-tile, then m-tile, and dealt out
 // round-robin to the CTAs: each output element is produced by exactly one
 // tile with a fixed k order, so the result does not depend on the grid size.
@@ -41,8 +43,9 @@ constexpr int B_STAGE_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr int ACC_BUFS = 2;
 constexpr int TMEM_COLS = ACC_BUFS * BN;  // 512 = all of tensor memory
-constexpr int NUM_THREADS = 192;
-constexpr int EPI_WARPS = 4;
+constexpr int EPI_WARP0 = 2;
+constexpr int EPI_WARPS = 8;                  // two per TMEM lane quarter
+constexpr int NUM_THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
 constexpr int SLOT = DMOE_SLOT_COLS;
 
 struct alignas(8) Ctrl {
@@ -58,7 +61,8 @@ struct alignas(8) Ctrl {
   int mt[DMOE_MAX_EXPERTS + 1];          // exclusive prefix of m-tiles per expert
 };
 
-constexpr size_t kSmemBytes = 1024 + size_t(STAGES) * STAGE_BYTES + sizeof(Ctrl);
+constexpr int STG_BYTES = 32 * 64;             // per epilogue warp: 32 rows x 32 bf16
+constexpr size_t kSmemBytes = 1024 + size_t(STAGES) * STAGE_BYTES + size_t(EPI_WARPS) * STG_BYTES + sizeof(Ctrl);
 
 struct KParams {
   const int32_t* offsets;
@@ -120,7 +124,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
                     const KParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Ctrl& c = *reinterpret_cast<Ctrl*>(base + size_t(STAGES) * STAGE_BYTES);
+  Ctrl& c = *reinterpret_cast<Ctrl*>(base + size_t(STAGES) * STAGE_BYTES + size_t(EPI_WARPS) * STG_BYTES);
   const uint32_t stage0 = smem_u32(base);
 
   const int tid = threadIdx.x;
@@ -251,63 +255,102 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
       mbar_wait_drain(smem_u32(&c.mma_done), 0);
     }
   } else {
-    // -------------------------------------------------- epilogue (4 warps)
-    const int q = warp & 3;               // TMEM lane quarter this warp may access
+    // -------------------------------------------------- epilogue (8 warps)
+    // Warp w may only read TMEM lanes 32*(w%4)..+31; warps 2-5 take the first
+    // 128 columns (one slot) of their lane quarter, warps 6-9 the second.
+    // tcgen05.ld gives one row per thread; each 32x32 bf16 chunk goes through
+    // a 2 KB swizzled shared-memory buffer so that four lanes cover 64
+    // contiguous bytes of a row: the expert_out stores and the grad_out
+    // gather then touch 8 rows per warp instruction instead of 32.
+    const int q = warp & 3;
+    const int h = (warp - EPI_WARP0) / 4;
+    const int k4 = lane & 3;                     // 16-byte piece of a 64-byte chunk row
+    const uint32_t stg = stage0 + uint32_t(STAGES * STAGE_BYTES + (warp - EPI_WARP0) * STG_BYTES);
     int acc = 0;
     uint32_t aph = 0;
     for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
       const Tile tl = decode_tile(t, c, E, p.NT);
-      if (!mbar_wait(smem_u32(&c.acc_full[acc]), aph, &c.abort, p.status)) break;
-      tc_fence_after();
-      const int r = tl.row0 + q * 32 + lane;
-      int src = 0, tok = 0;
-      bool valid = r < tl.row_end;
-      if (MODE != int(GemmMode::kFwd) && valid) {
-        src = p.row_src[r];
-        if (unsigned(src) >= unsigned(p.R)) {   // corrupt row_src: report, never index with it
-          record_error(p.status, DMOE_ERR_ROUTING);
-          valid = false;
-        }
-        tok = src / p.topk;
+      const int col0 = tl.n0 + h * SLOT;
+      const bool active = col0 < p.N;           // warp-uniform: a half-width last N-tile
+      // rows of this lane in the coalesced layout: q*32 + i*8 + lane/4, i = 0..3
+      int rr[4], src[4];
+      bool ok[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        rr[i] = tl.row0 + q * 32 + i * 8 + (lane >> 2);
+        ok[i] = active && rr[i] < tl.row_end;
+        src[i] = 0;
       }
-      const uint32_t tbase = tmem_base + uint32_t(acc * BN) + (uint32_t(q * 32) << 16);
-#pragma unroll 1
-      for (int h = 0; h < BN / SLOT; ++h) {
-        const int col0 = tl.n0 + h * SLOT;
-        if (col0 >= p.N) break;
-        float a[8];
+      // Prefetch grad_out for all four rows before the accumulator is ready.
+      uint4 g[16];
+      if (MODE != int(GemmMode::kFwd)) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) a[j] = 0.0f;
-#pragma unroll
-        for (int ch = 0; ch < SLOT / 32; ++ch) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tbase + uint32_t(h * SLOT + ch * 32), v);
-          tmem_wait_ld();
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2_rn(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-          if (valid) {
-            uint16_t* dst = p.out + size_t(r) * p.N + col0 + ch * 32;
-#pragma unroll
-            for (int vv = 0; vv < 4; ++vv)
-              stg_v4(dst + vv * 8, make_uint4(pk[4 * vv], pk[4 * vv + 1], pk[4 * vv + 2], pk[4 * vv + 3]));
-            if (MODE != int(GemmMode::kFwd)) {
-              const uint16_t* g = p.grad_out + size_t(tok) * p.N + col0 + ch * 32;
-#pragma unroll
-              for (int vv = 0; vv < 4; ++vv) {
-                const uint4 gv = ldg_nc_v4(g + vv * 8);
-                slot_accumulate8(a, gv, make_uint4(pk[4 * vv], pk[4 * vv + 1], pk[4 * vv + 2], pk[4 * vv + 3]));
-              }
+        for (int i = 0; i < 4; ++i) {
+          if (ok[i]) {
+            src[i] = p.row_src[rr[i]];
+            if (unsigned(src[i]) >= unsigned(p.R)) {   // corrupt row_src: report, never index with it
+              record_error(p.status, DMOE_ERR_ROUTING);
+              ok[i] = false;
             }
           }
         }
-        if (MODE != int(GemmMode::kFwd) && valid) {
-          const float part = slot_tree(a);
-          const int s = col0 / SLOT;
-          if (MODE == int(GemmMode::kSlots))
-            p.slots[size_t(s) * p.R + r] = part;
-          else
-            atomicAdd(p.dprob + src, part);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint16_t* gp = p.grad_out + size_t(ok[i] ? src[i] / p.topk : 0) * p.N + (ok[i] ? col0 : 0) + k4 * 8;
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) g[ch * 4 + i] = ok[i] ? ldg_nc_v4(gp + ch * 32) : make_uint4(0, 0, 0, 0);
+        }
+      }
+      if (!mbar_wait(smem_u32(&c.acc_full[acc]), aph, &c.abort, p.status)) break;
+      tc_fence_after();
+      if (active) {
+        const uint32_t tcol = tmem_base + uint32_t(acc * BN + h * SLOT) + (uint32_t(q * 32) << 16);
+        float a[4][8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) a[i][j] = 0.0f;
+#pragma unroll
+        for (int ch = 0; ch < SLOT / 32; ++ch) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tcol + uint32_t(ch * 32), v);
+          tmem_wait_ld();
+          // row `lane` of the chunk -> staging, piece kk at slot kk ^ ((row >> 1) & 3)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            uint4 y;
+            y.x = pack_bf16x2_rn(__uint_as_float(v[8 * kk + 0]), __uint_as_float(v[8 * kk + 1]));
+            y.y = pack_bf16x2_rn(__uint_as_float(v[8 * kk + 2]), __uint_as_float(v[8 * kk + 3]));
+            y.z = pack_bf16x2_rn(__uint_as_float(v[8 * kk + 4]), __uint_as_float(v[8 * kk + 5]));
+            y.w = pack_bf16x2_rn(__uint_as_float(v[8 * kk + 6]), __uint_as_float(v[8 * kk + 7]));
+            sts_v4(stg + uint32_t(lane * 64 + ((kk ^ ((lane >> 1) & 3)) << 4)), y);
+          }
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int row = i * 8 + (lane >> 2);
+            const uint4 y = lds_v4(stg + uint32_t(row * 64 + ((k4 ^ ((row >> 1) & 3)) << 4)));
+            if (ok[i]) {
+              stg_v4(p.out + size_t(rr[i]) * p.N + col0 + ch * 32 + k4 * 8, y);
+              if (MODE != int(GemmMode::kFwd)) slot_accumulate8(a[i], g[ch * 4 + i], y);
+            }
+          }
+          __syncwarp();
+        }
+        if (MODE != int(GemmMode::kFwd)) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            // part k4 of row rr[i]; combine the four parts as (L0 + L1) + (L2 + L3)
+            float part = slot_tree(a[i]);
+            part = __fadd_rn(part, __shfl_xor_sync(0xffffffffu, part, 1));
+            part = __fadd_rn(part, __shfl_xor_sync(0xffffffffu, part, 2));
+            if (k4 == 0 && ok[i]) {
+              if (MODE == int(GemmMode::kSlots))
+                p.slots[size_t(col0 / SLOT) * p.R + rr[i]] = part;
+              else
+                atomicAdd(p.dprob + src[i], part);
+            }
+          }
         }
       }
       tc_fence_before();

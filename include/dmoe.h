@@ -128,10 +128,13 @@ dmoe_status moe_grouped_gemm_fwd(const void* X_perm, const void* W, const int32_
  * combine (the deterministic path).  Besides expert_out as above:
  *     slots[s, r] = sum over the 128 columns n of slot s of
  *                   float(grad_out[t(r), n]) * float(expert_out[r, n])
- * using the STORED bf16 expert_out value, summed in this fixed tree: eight
- * fp32 partials a_j = sum_{i=0..15} p[8i+j] (i ascending, fused multiply-add
- * from +0), then ((a0+a1)+(a2+a3))+((a4+a5)+(a6+a7)).  Each N-tile writes
- * only its own slots.  Then, after all writers are done,
+ * using the STORED bf16 expert_out value, summed in this fixed tree: the
+ * slot's 16 groups of 8 columns are split into four parts k = g mod 4; part k
+ * keeps eight fp32 partials a_j = sum over its groups g = k, k+4, k+8, k+12
+ * (ascending) of p[8g+j] (fused multiply-add from +0) and folds them as
+ * L_k = ((a0+a1)+(a2+a3))+((a4+a5)+(a6+a7)); the slot value is
+ * (L_0+L_1)+(L_2+L_3).  Each N-tile writes only its own slots.  Then, after
+ * all writers are done,
  *     dprob[row_src[r]] = (((slots[0,r] + slots[1,r]) + slots[2,r]) + ...)
  * in ascending slot order, fp32.
  *   grad_out  bf16 [T, N]      gradient at the expert-combine output, by token
