@@ -66,7 +66,10 @@ dmoe_status cuda_status(cudaError_t e) {
   return DMOE_ERR_CUDA;
 }
 
+// Workspace status region: status word at byte 0, the GEMM's dynamic tile
+// counters (two ints, left at zero by every launch) at byte 64.
 int* status_ptr(void* ws) { return static_cast<int*>(ws); }
+int* sched_ptr(void* ws) { return reinterpret_cast<int*>(static_cast<char*>(ws) + 64); }
 
 dmoe_status check_gemm_shape(const void* X, const void* W, const int32_t* off, int R, int E, int K, int N,
                              const void* out, void* ws, size_t ws_bytes) {
@@ -146,6 +149,7 @@ dmoe_status moe_grouped_gemm_fwd(const void* X_perm, const void* W, const int32_
   a.R = R; a.E = E; a.K = K; a.N = N;
   a.out = expert_out;
   a.status = status_ptr(ws);
+  a.sched = sched_ptr(ws);
   a.num_ctas = launch ? launch->num_ctas : 0;
   if (a.num_ctas < 0) return DMOE_ERR_INVALID_ARG;
   return cuda_status(launch_grouped_gemm(GemmMode::kFwd, a, reinterpret_cast<cudaStream_t>(stream)));
@@ -175,6 +179,7 @@ dmoe_status moe_grouped_gemm_dprob(const void* X_perm, const void* W, const int3
   a.grad_out = grad_out; a.row_src = row_src; a.topk = topk;
   a.slots = slots;
   a.status = status_ptr(ws);
+  a.sched = sched_ptr(ws);
   a.num_ctas = launch ? launch->num_ctas : 0;
   if (a.num_ctas < 0) return DMOE_ERR_INVALID_ARG;
   cudaError_t e = launch_grouped_gemm(GemmMode::kSlots, a, s);
@@ -204,6 +209,7 @@ dmoe_status moe_grouped_gemm_dprob_atomic(const void* X_perm, const void* W, con
   a.grad_out = grad_out; a.row_src = row_src; a.topk = topk;
   a.dprob = dprob;
   a.status = status_ptr(ws);
+  a.sched = sched_ptr(ws);
   a.num_ctas = launch ? launch->num_ctas : 0;
   if (a.num_ctas < 0) return DMOE_ERR_INVALID_ARG;
   return cuda_status(launch_grouped_gemm(GemmMode::kAtomic, a, s));

@@ -6,7 +6,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
-#include "../../include/dmoe.h"
+#include "dmoe.h"
 
 namespace dmoe {
 
@@ -68,6 +68,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
       }
     }
   }
+}
+
+// Warp-uniform variant: lane 0 waits, the outcome is broadcast, and the
+// __syncwarp orders the other lanes' later reads after the completed phase.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort, int* status,
+                                          int lane) {
+  int ok = 1;
+  if (lane == 0) ok = mbar_wait(bar, parity, abort, status) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok != 0;
 }
 
 // Same, with its own (shorter) limit and no abort flag: used on the unwind
@@ -232,6 +243,21 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p));
   return v;
+}
+
+// Same loads/stores with an L2 eviction-priority policy (from createpolicy).
+__device__ __forceinline__ uint4 ldg_nc_v4_hint(const void* p, uint64_t policy) {
+  uint4 v;
+  asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(policy));
+  return v;
+}
+
+__device__ __forceinline__ void stg_v4_hint(void* p, const uint4& v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w), "l"(policy)
+               : "memory");
 }
 
 __device__ __forceinline__ void sts_v4(uint32_t addr, const uint4& v) {

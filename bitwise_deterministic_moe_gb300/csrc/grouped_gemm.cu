@@ -20,9 +20,10 @@
 //           grad_out in the fixed tree (one thread per output row; one warp
 //           per 32 rows x 128 columns = one private slot).  The row's
 //           grad_out slice is fetched before the accumulator is ready.
-// Tiles are enumerated expert-major, then n-tile, then m-tile, and dealt out
-// round-robin to the CTAs: each output element is produced by exactly one
-// tile with a fixed k order, so the result does not depend on the grid size.
+// Tiles are enumerated expert-major, then n-tile, then m-tile, and handed out
+// dynamically (a global counter): each output element is produced by exactly
+// one tile with a fixed k order, so the result does not depend on which CTA
+// runs it or on the grid size.
 // An M-tile may run past its expert's last row into the next expert's rows;
 // those rows are computed but never stored.
 #include <cuda.h>
@@ -47,6 +48,7 @@ constexpr int EPI_WARP0 = 2;
 constexpr int EPI_WARPS = 8;                  // two per TMEM lane quarter
 constexpr int NUM_THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
 constexpr int SLOT = DMOE_SLOT_COLS;
+constexpr int TQ = 4;                         // tile-queue depth (producer runs <= 3 tiles ahead)
 
 struct alignas(8) Ctrl {
   uint64_t full[STAGES];
@@ -54,6 +56,9 @@ struct alignas(8) Ctrl {
   uint64_t acc_full[ACC_BUFS];
   uint64_t acc_empty[ACC_BUFS];
   uint64_t mma_done;
+  uint64_t tq_full[TQ];                  // tile queue: producer -> MMA + epilogue
+  uint64_t tq_empty[TQ];                 // slot consumed by the MMA thread and all epilogue warps
+  int tq_tile[TQ];                       // tile index, -1 = no more tiles
   uint32_t tmem_base;
   int abort;
   int bad;
@@ -74,6 +79,7 @@ struct KParams {
   float* slots;
   float* dprob;
   int* status;
+  int* sched;   // [0] next-tile counter, [1] finished-CTA counter; zero between launches
 };
 
 // Shared-memory matrix descriptor for a K-major operand tile written by TMA
@@ -142,6 +148,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
       mbar_init(smem_u32(&c.acc_empty[b]), EPI_WARPS);
     }
     mbar_init(smem_u32(&c.mma_done), 1);
+    for (int i = 0; i < TQ; ++i) {
+      mbar_init(smem_u32(&c.tq_full[i]), 1);
+      mbar_init(smem_u32(&c.tq_empty[i]), 1 + EPI_WARPS);
+    }
     c.abort = 0;
     c.bad = 0;
     fence_barrier_init();
@@ -199,8 +209,20 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
       for (int s = 0; s < STAGES; ++s) issued[s] = 0;
       int stage = 0;
       uint32_t ph = 0;
-      for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
-        const Tile tl = decode_tile(t, c, E, p.NT);
+      // Tiles are handed out dynamically (first tile = blockIdx.x, then a
+      // global counter), so neighbouring tiles -- which share weight slices
+      // and X rows in L2 -- run at nearly the same time on different SMs.
+      // Which CTA computes a tile never changes its bits.
+      int tile = blockIdx.x;
+      for (int qi = 0;; ++qi) {
+        const int qs = qi % TQ;
+        if (!mbar_wait(smem_u32(&c.tq_empty[qs]), uint32_t((qi / TQ) & 1) ^ 1u, &c.abort, p.status)) break;
+        const int cur = tile < total_tiles ? tile : -1;
+        c.tq_tile[qs] = cur;
+        mbar_arrive(smem_u32(&c.tq_full[qs]));
+        if (cur < 0) break;
+        tile = int(gridDim.x) + atomicAdd(p.sched, 1);   // fetched early: latency hides behind the loads
+        const Tile tl = decode_tile(cur, c, E, p.NT);
         const int brow = tl.e * p.N + tl.n0;
         bool ok = true;
         for (int kb = 0; kb < p.KB; ++kb) {
@@ -226,7 +248,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
       uint32_t ph = 0;
       int acc = 0;
       uint32_t aph = 0;
-      for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+      for (int qi = 0;; ++qi) {
+        const int qs = qi % TQ;
+        if (!mbar_wait(smem_u32(&c.tq_full[qs]), uint32_t((qi / TQ) & 1), &c.abort, p.status)) break;
+        const int cur = c.tq_tile[qs];
+        mbar_arrive(smem_u32(&c.tq_empty[qs]));
+        if (cur < 0) break;
         if (!mbar_wait(smem_u32(&c.acc_empty[acc]), aph ^ 1u, &c.abort, p.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
@@ -265,11 +292,20 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
     const int q = warp & 3;
     const int h = (warp - EPI_WARP0) / 4;
     const int k4 = lane & 3;                     // 16-byte piece of a 64-byte chunk row
+    // grad_out rows are gathered 8x per token and slot: ask L2 to keep them
+    // while 2+ GB of weights stream past.
+    const uint64_t pol_keep = policy_evict_last();
     const uint32_t stg = stage0 + uint32_t(STAGES * STAGE_BYTES + (warp - EPI_WARP0) * STG_BYTES);
     int acc = 0;
     uint32_t aph = 0;
-    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
-      const Tile tl = decode_tile(t, c, E, p.NT);
+    for (int qi = 0;; ++qi) {
+      const int qs = qi % TQ;
+      if (!warp_wait(smem_u32(&c.tq_full[qs]), uint32_t((qi / TQ) & 1), &c.abort, p.status, lane)) break;
+      const int cur = c.tq_tile[qs];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&c.tq_empty[qs]));
+      if (cur < 0) break;
+      const Tile tl = decode_tile(cur, c, E, p.NT);
       const int col0 = tl.n0 + h * SLOT;
       const bool active = col0 < p.N;           // warp-uniform: a half-width last N-tile
       // rows of this lane in the coalesced layout: q*32 + i*8 + lane/4, i = 0..3
@@ -298,10 +334,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
         for (int i = 0; i < 4; ++i) {
           const uint16_t* gp = p.grad_out + size_t(ok[i] ? src[i] / p.topk : 0) * p.N + (ok[i] ? col0 : 0) + k4 * 8;
 #pragma unroll
-          for (int ch = 0; ch < 4; ++ch) g[ch * 4 + i] = ok[i] ? ldg_nc_v4(gp + ch * 32) : make_uint4(0, 0, 0, 0);
+          for (int ch = 0; ch < 4; ++ch) g[ch * 4 + i] = ok[i] ? ldg_nc_v4_hint(gp + ch * 32, pol_keep) : make_uint4(0, 0, 0, 0);
         }
       }
-      if (!mbar_wait(smem_u32(&c.acc_full[acc]), aph, &c.abort, p.status)) break;
+      if (!warp_wait(smem_u32(&c.acc_full[acc]), aph, &c.abort, p.status, lane)) break;
       tc_fence_after();
       if (active) {
         const uint32_t tcol = tmem_base + uint32_t(acc * BN + h * SLOT) + (uint32_t(q * 32) << 16);
@@ -365,6 +401,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+  if (tid == 0) {
+    // this thread made the CTA's last counter fetch; the last CTA to finish
+    // zeroes both counters for the next launch on this stream
+    __threadfence();
+    if (atomicAdd(p.sched + 1, 1) == int(gridDim.x) - 1) {
+      atomicExch(p.sched, 0);
+      atomicExch(p.sched + 1, 0);
+    }
   }
 }
 
@@ -436,6 +481,8 @@ cudaError_t launch_grouped_gemm(GemmMode mode, const GemmArgs& a, cudaStream_t s
   kp.slots = a.slots;
   kp.dprob = a.dprob;
   kp.status = a.status;
+  kp.sched = a.sched;
+  if (!kp.sched) return cudaErrorInvalidValue;
   int grid = a.num_ctas > 0 ? a.num_ctas : device_sm_count();
   switch (mode) {
     case GemmMode::kFwd: return launch_mode<int(GemmMode::kFwd)>(ta, tb, kp, grid, stream);

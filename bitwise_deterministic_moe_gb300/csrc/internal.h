@@ -22,7 +22,8 @@ struct GemmArgs {
   int topk;
   float* slots;               // [S, R]        (slots)
   float* dprob;               // [T*topk]      (atomic)
-  int* status;                // device status word
+  int* status;                // device status word (may be null: errors not recorded)
+  int* sched;                 // 2 device ints, zero between launches: dynamic tile counter
   int num_ctas;               // 0 = one per SM
 };
 

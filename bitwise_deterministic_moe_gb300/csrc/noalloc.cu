@@ -28,13 +28,16 @@ namespace {
 constexpr size_t kNoallocSlotFloats = size_t(DMOE_NOALLOC_MAX_SLOT_VALUES);
 
 static __device__ __align__(256) float g_noalloc_slots[kNoallocSlotFloats];
+// the grouped GEMM's dynamic tile counters; zero at load, left at zero by every launch
+static __device__ __align__(256) int g_noalloc_sched[2];
 
-// Device address of g_noalloc_slots for the current device.  In host code the
+// Device addresses of g_noalloc_slots and g_noalloc_sched for the current device.  In host code the
 // symbol's name is only a host-side stand-in, so the real address is fetched
 // once per device with that device current.
-cudaError_t noalloc_slots_ptr(float** out) {
+cudaError_t noalloc_ptrs(float** slots_out, int** sched_out) {
   static std::mutex mu;
   static float* ptrs[64] = {nullptr};
+  static int* sched[64] = {nullptr};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -44,9 +47,14 @@ cudaError_t noalloc_slots_ptr(float** out) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_slots);
     if (e != cudaSuccess) return e;
+    void* q = nullptr;
+    e = cudaGetSymbolAddress(&q, g_noalloc_sched);
+    if (e != cudaSuccess) return e;
     ptrs[dev] = static_cast<float*>(p);
+    sched[dev] = static_cast<int*>(q);
   }
-  *out = ptrs[dev];
+  *slots_out = ptrs[dev];
+  *sched_out = sched[dev];
   return cudaSuccess;
 }
 
@@ -75,7 +83,8 @@ extern "C" dmoe_status moe_grouped_gemm_dprob_noalloc(const void* X_perm, const 
   if (launch && launch->num_ctas < 0) return DMOE_ERR_INVALID_ARG;
 
   float* slots = nullptr;
-  if (noalloc_slots_ptr(&slots) != cudaSuccess) return DMOE_ERR_CUDA;
+  int* sched = nullptr;
+  if (noalloc_ptrs(&slots, &sched) != cudaSuccess) return DMOE_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   GemmArgs a{};
   a.X = X_perm; a.W = W; a.offsets = expert_offsets;
@@ -84,6 +93,7 @@ extern "C" dmoe_status moe_grouped_gemm_dprob_noalloc(const void* X_perm, const 
   a.grad_out = grad_out; a.row_src = row_src; a.topk = topk;
   a.slots = slots;
   a.status = nullptr;   // no caller workspace: device-side errors are not recorded
+  a.sched = sched;
   a.num_ctas = launch ? launch->num_ctas : 0;
   if (launch_grouped_gemm(GemmMode::kSlots, a, s) != cudaSuccess) return DMOE_ERR_CUDA;
   if (launch_dprob_combine(slots, row_src, R, S, dprob, s) != cudaSuccess) return DMOE_ERR_CUDA;

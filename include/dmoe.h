@@ -31,7 +31,9 @@
  *    are written to the status word at the start of the workspace `ws` and
  *    read back with dmoe_read_status().
  *  - Results are bitwise identical for any num_ctas >= 1, any stream, and
- *    any number of concurrent calls on separate output buffers.
+ *    any number of concurrent calls on separate output buffers and separate
+ *    workspaces.  A workspace holds the grouped GEMM's dynamic tile counter:
+ *    calls that share one must be ordered on one stream.
  */
 #ifndef DMOE_H_
 #define DMOE_H_
@@ -80,9 +82,10 @@ const char* dmoe_status_string(int status);
 int dmoe_version(void);
 
 /* Workspace needed by every call below for a problem with T tokens, topk
- * choices and E experts (routing scratch + the status word).  The caller
- * allocates it once, ZERO-FILLED, and may reuse it for every call on that
- * problem size; calls that share a workspace must be ordered on one stream. */
+ * choices and E experts (status word, the grouped GEMM's tile counters, and
+ * routing scratch).  The caller allocates it once, ZERO-FILLED, and may reuse
+ * it for every call on that problem size; every call leaves the counters at
+ * zero.  Calls that share a workspace must be ordered on one stream. */
 size_t dmoe_workspace_bytes(int T, int topk, int E);
 
 /* Reads (synchronising `stream`) and clears the device status word in ws.

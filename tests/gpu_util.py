@@ -38,8 +38,9 @@ class Problem:
         self.ws = api.workspace(cfg.T, cfg.topk, cfg.E, dev)
         self.off, self.src = api.permute_indices(self.ids, cfg.E, self.ws)
 
-    def run_dprob(self, num_ctas=0, stream=None, out=None, slots=None, dprob=None):
-        return api.grouped_gemm_dprob(self.X, self.W, self.off, self.G, self.src, self.cfg.topk, self.ws,
+    def run_dprob(self, num_ctas=0, stream=None, out=None, slots=None, dprob=None, ws=None):
+        return api.grouped_gemm_dprob(self.X, self.W, self.off, self.G, self.src, self.cfg.topk,
+                                      self.ws if ws is None else ws,
                                       out=out, slots=slots, dprob=dprob, num_ctas=num_ctas, stream=stream)
 
 

@@ -50,14 +50,15 @@ def test_stress_100_launches_3_grids_2_streams():
     ref = fps(out, slots, dprob)
     streams = [torch.cuda.Stream(), torch.cuda.Stream()]
     bufs = [prob.run_dprob() for _ in streams]          # separate outputs per stream
+    wss = [api.workspace(cfg.T, cfg.topk, cfg.E) for _ in streams]   # and separate workspaces
     torch.cuda.synchronize()
     mismatches = 0
     launches = 0
     for it in range(100 // 2):
         for grid in (sms, sms // 2, 37):
-            for s, (o, d, sl) in zip(streams, bufs):
+            for s, (o, d, sl), w in zip(streams, bufs, wss):
                 with torch.cuda.stream(s):
-                    prob.run_dprob(num_ctas=grid, out=o, slots=sl, dprob=d, stream=s)
+                    prob.run_dprob(num_ctas=grid, out=o, slots=sl, dprob=d, stream=s, ws=w)
                 launches += 1
             if it % 10 == 0 or it == 100 // 2 - 1:
                 torch.cuda.synchronize()
@@ -69,6 +70,8 @@ def test_stress_100_launches_3_grids_2_streams():
     assert launches == 300
     assert mismatches == 0
     assert api.read_status(prob.ws) == 0
+    for w in wss:
+        assert api.read_status(w) == 0
 
 
 def test_atomic_control_differs_run_to_run_is_recorded():
