@@ -27,7 +27,7 @@ namespace dmoe {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr size_t kPartBytes = 64 * 1024;   // bytes of one chunk handled by one CTA
+constexpr size_t kPartBytes = 16 * 1024;   // bytes of one chunk handled by one CTA
 
 __device__ __forceinline__ uint32_t fmix32(uint32_t h) {
   h ^= h >> 16;

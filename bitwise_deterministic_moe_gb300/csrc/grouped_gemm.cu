@@ -20,10 +20,11 @@
 //           grad_out in the fixed tree (one thread per output row; one warp
 //           per 32 rows x 128 columns = one private slot).  The row's
 //           grad_out slice is fetched before the accumulator is ready.
-// Tiles are enumerated expert-major, then n-tile, then m-tile, and handed out
-// dynamically (a global counter): each output element is produced by exactly
-// one tile with a fixed k order, so the result does not depend on which CTA
-// runs it or on the grid size.
+// Tiles (one m-tile x one n-tile of one expert) are ordered so that heavy and
+// light experts' work interleaves (see decode_tile) and handed out dynamically
+// through a global counter: each output element is produced by exactly one
+// tile with a fixed k order, so the result does not depend on which CTA runs
+// it, on the order, or on the grid size.
 // An M-tile may run past its expert's last row into the next expert's rows;
 // those rows are computed but never stored.
 #include <cuda.h>
@@ -49,6 +50,7 @@ constexpr int EPI_WARPS = 8;                  // two per TMEM lane quarter
 constexpr int NUM_THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
 constexpr int SLOT = DMOE_SLOT_COLS;
 constexpr int TQ = 4;                         // tile-queue depth (producer runs <= 3 tiles ahead)
+constexpr int HEAVY_MT = 3;                   // experts with >= 3 m-tiles reuse each weight slice 3+ times
 
 struct alignas(8) Ctrl {
   uint64_t full[STAGES];
@@ -63,7 +65,8 @@ struct alignas(8) Ctrl {
   int abort;
   int bad;
   int off[DMOE_MAX_EXPERTS + 1];         // expert row offsets
-  int mt[DMOE_MAX_EXPERTS + 1];          // exclusive prefix of m-tiles per expert
+  int hp[DMOE_MAX_EXPERTS + 1];          // exclusive prefix of m-tiles of heavy experts (0 for light ones)
+  int cp[DMOE_MAX_EXPERTS + 1];          // exclusive prefix of m-tiles of light experts (0 for heavy ones)
 };
 
 constexpr int STG_BYTES = 32 * 64;             // per epilogue warp: 32 rows x 32 bf16
@@ -105,20 +108,30 @@ struct Tile {
   int e, row0, row_end, n0;
 };
 
-__device__ __forceinline__ Tile decode_tile(int t, const Ctrl& c, int E, int NT) {
-  // largest e in [0, E) with mt[e] * NT <= t  (skips empty experts)
+// Tile order.  A unit is one m-tile of one expert; its NT n-tiles are
+// consecutive tiles (they share the X rows in L2).  Units of heavy experts
+// (compute-bound: each weight slice serves >= HEAVY_MT m-tiles) and of light
+// experts (bound by streaming their weights from HBM) are merged in
+// proportion -- unit position p is heavy iff floor((p+1)H/U) > floor(pH/U) --
+// so both the tensor cores and HBM stay busy; within each class units follow
+// expert order, so an expert's weight slices are reused while resident.
+// The order only decides when a tile runs, never what it computes.
+__device__ __forceinline__ Tile decode_tile(int t, const Ctrl& c, int E, int NT, int H, int U) {
+  const int p = t / NT;
+  const int n_tile = t - p * NT;
+  const int i = int((long long)p * H / U);                   // heavy units before position p
+  const bool heavy = (long long)(p + 1) * H / U > i;
+  const int* pre = heavy ? c.hp : c.cp;
+  const int u = heavy ? i : p - i;
+  // largest e in [0, E) with pre[e] <= u (skips experts of the other class and empty ones)
   int lo = 0, hi = E;
   while (hi - lo > 1) {
     int mid = (lo + hi) >> 1;
-    if (c.mt[mid] * NT <= t) lo = mid; else hi = mid;
+    if (pre[mid] <= u) lo = mid; else hi = mid;
   }
-  int mtiles = c.mt[lo + 1] - c.mt[lo];
-  int local = t - c.mt[lo] * NT;
-  int n_tile = local / mtiles;
-  int m_tile = local - n_tile * mtiles;
   Tile tl;
   tl.e = lo;
-  tl.row0 = c.off[lo] + m_tile * BM;
+  tl.row0 = c.off[lo] + (u - pre[lo]) * BM;
   tl.row_end = c.off[lo + 1];
   tl.n0 = n_tile * BN;
   return tl;
@@ -172,25 +185,29 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
   for (int e = tid; e < E; e += NUM_THREADS) {
     int a = c.off[e], b = c.off[e + 1];
     if (b < a) bad = 1;
-    c.mt[e + 1] = (b > a) ? (b - a + BM - 1) / BM : 0;
+    const int mt = (b > a) ? (b - a + BM - 1) / BM : 0;
+    c.hp[e + 1] = mt >= HEAVY_MT ? mt : 0;
+    c.cp[e + 1] = mt >= HEAVY_MT ? 0 : mt;
   }
   if (tid == 0) {
     if (c.off[0] != 0 || c.off[E] != p.R) bad = 1;
-    c.mt[0] = 0;
+    c.hp[0] = 0;
+    c.cp[0] = 0;
   }
   bad = __syncthreads_or(bad);
-  if (warp == 0) {
-    // inclusive scan of mt[1..E] in chunks of 32 (mt[0] = 0)
+  if (warp < 2) {
+    // inclusive scans of hp[1..E] (warp 0) and cp[1..E] (warp 1) in chunks of 32
+    int* pre = warp == 0 ? c.hp : c.cp;
     int carry = 0;
     for (int b0 = 1; b0 <= E; b0 += 32) {
       int i = b0 + lane;
-      int v = (i <= E) ? c.mt[i] : 0;
+      int v = (i <= E) ? pre[i] : 0;
 #pragma unroll
       for (int d = 1; d < 32; d <<= 1) {
         int u = __shfl_up_sync(0xffffffffu, v, d);
         if (lane >= d) v += u;
       }
-      if (i <= E) c.mt[i] = v + carry;
+      if (i <= E) pre[i] = v + carry;
       carry += __shfl_sync(0xffffffffu, v, 31);
     }
   }
@@ -198,7 +215,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
   __syncthreads();
   tc_fence_after();
   if (bad && tid == 0) record_error(p.status, DMOE_ERR_ROUTING);
-  const int total_tiles = bad ? 0 : c.mt[E] * p.NT;
+  const int units_heavy = c.hp[E];
+  const int units = c.hp[E] + c.cp[E];
+  const int total_tiles = bad ? 0 : units * p.NT;
   const uint32_t tmem_base = c.tmem_base;
 
   if (warp == 0) {
@@ -222,7 +241,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
         mbar_arrive(smem_u32(&c.tq_full[qs]));
         if (cur < 0) break;
         tile = int(gridDim.x) + atomicAdd(p.sched, 1);   // fetched early: latency hides behind the loads
-        const Tile tl = decode_tile(cur, c, E, p.NT);
+        const Tile tl = decode_tile(cur, c, E, p.NT, units_heavy, units);
         const int brow = tl.e * p.N + tl.n0;
         bool ok = true;
         for (int kb = 0; kb < p.KB; ++kb) {
@@ -305,7 +324,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&c.tq_empty[qs]));
       if (cur < 0) break;
-      const Tile tl = decode_tile(cur, c, E, p.NT);
+      const Tile tl = decode_tile(cur, c, E, p.NT, units_heavy, units);
       const int col0 = tl.n0 + h * SLOT;
       const bool active = col0 < p.N;           // warp-uniform: a half-width last N-tile
       // rows of this lane in the coalesced layout: q*32 + i*8 + lane/4, i = 0..3

@@ -5,8 +5,9 @@
 // bit à bit de Megatron Core à 2432 GPU ...", section "Méthodologie de
 // débogage du non-déterminisme"), so every position is derived from counts and
 // prefix sums, never from atomic position tickets:
-//   1. histogram: one warp per block of 1024 entries counts ids per expert
-//      (integer counts are order-independent);
+//   1. histogram: one warp per block of 1024 entries (all 32 loads per lane
+//      issued up front) counts ids per expert (integer counts are
+//      order-independent);
 //   2. block scan: one warp per expert turns its per-block counts into
 //      exclusive prefixes (within-expert rank base of each block);
 //   3. expert scan: one CTA scans the per-expert totals into expert_offsets;
@@ -29,18 +30,27 @@ hist_kernel(const int32_t* __restrict__ ids, long long R, int E, int nblk, int32
   const int lane = threadIdx.x;
   const int b = blockIdx.x;
   for (int e = lane; e < E; e += 32) cnt[e] = 0;
+  // all 32 loads of this lane in flight at once (the block is latency-bound)
+  const long long i0 = (long long)b * kEntriesPerBlock + lane;
+  int v[kEntriesPerBlock / 32];
+#pragma unroll
+  for (int k = 0; k < kEntriesPerBlock / 32; ++k) {
+    const long long i = i0 + 32ll * k;
+    v[k] = (i < R) ? __ldg(ids + i) : 0;
+  }
   __syncwarp();
-  const long long i0 = (long long)b * kEntriesPerBlock;
-  for (int k = lane; k < kEntriesPerBlock; k += 32) {
-    long long i = i0 + k;
-    if (i >= R) break;
-    int e = ids[i];
+  bool bad = false;
+#pragma unroll
+  for (int k = 0; k < kEntriesPerBlock / 32; ++k) {
+    if (i0 + 32ll * k >= R) continue;
+    const int e = v[k];
     if (e < 0 || e >= E) {
-      record_error(status, DMOE_ERR_ROUTING);
+      bad = true;
       continue;
     }
     atomicAdd(&cnt[e], 1);
   }
+  if (bad) record_error(status, DMOE_ERR_ROUTING);
   __syncwarp();
   for (int e = lane; e < E; e += 32) counts[(size_t)e * nblk + b] = cnt[e];
 }
@@ -105,18 +115,25 @@ scatter_kernel(const int32_t* __restrict__ ids, long long R, int E, int nblk, co
   __shared__ int next[DMOE_MAX_EXPERTS];
   const int lane = threadIdx.x;
   const int b = blockIdx.x;
+  const long long i0 = (long long)b * kEntriesPerBlock + lane;
+  int v[kEntriesPerBlock / 32];
+#pragma unroll
+  for (int k = 0; k < kEntriesPerBlock / 32; ++k) {
+    const long long i = i0 + 32ll * k;
+    v[k] = (i < R) ? __ldg(ids + i) : -1;
+  }
   for (int e = lane; e < E; e += 32) next[e] = offsets[e] + counts[(size_t)e * nblk + b];
   __syncwarp();
   const unsigned lt = (1u << lane) - 1u;
-  const long long i0 = (long long)b * kEntriesPerBlock;
-  for (int k0 = 0; k0 < kEntriesPerBlock; k0 += 32) {
-    const long long i = i0 + k0 + lane;
-    int e = (i < R) ? ids[i] : -1;
+#pragma unroll
+  for (int k = 0; k < kEntriesPerBlock / 32; ++k) {
+    const long long i = i0 + 32ll * k;
+    int e = v[k];
     const bool ok = e >= 0 && e < E;
     if (!ok) e = -1;
     const unsigned peers = __match_any_sync(0xffffffffu, e);
     const int rank = __popc(peers & lt);
-    int base = ok ? next[e] : 0;
+    const int base = ok ? next[e] : 0;
     __syncwarp();
     if (ok) {
       row_src[base + rank] = (int32_t)i;
