@@ -137,6 +137,24 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
+def max_over_ranks(x: float, world: int) -> float:
+    """The slowest rank's time (host all-reduce over gloo; replicas exchange
+    nothing else)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_step: float, steps: int, world: int, ms_max: float) -> float:
+    """Units all ranks processed over the slowest rank's time (weak scaling:
+    every replica runs the full workload)."""
+    return world * flops_per_step * steps / (ms_max * 1e-3) / 1e12
+
+
 def cpu_baseline(cfg, inp, target_s=12.0):
     """The oracle as it stands, timed on this host's cores on a bounded sample
     of rows of the same workload (GEMM + bf16 rounding + slot partials + dprob)."""
@@ -289,13 +307,9 @@ def run_ours(args):
     gemm_ms = float(np.mean([a.elapsed_time(b) for a, b in gemm_ev]))
     if api.read_status(ws) != 0:
         raise RuntimeError("device status set during the timed region")
-    ms_max = ms
-    if world > 1:
-        tt = torch.tensor([ms], dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_max = float(tt.item())
+    ms_max = max_over_ranks(ms, world)
     ms_per_step = ms_max / args.steps
-    value = world * flops * args.steps / (ms_max * 1e-3) / 1e12
+    value = whole_job_tflops(flops, args.steps, world, ms_max)
 
     # ---------------- determinism tax: deterministic call vs atomic control
     def timed(fn, iters):
@@ -366,14 +380,10 @@ def run_ours(args):
             e2e_step()
         b.record(stream)
         torch.cuda.synchronize(dev)
-        e_ms = a.elapsed_time(b)
-        if world > 1:
-            tt = torch.tensor([e_ms], dtype=torch.float64)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e_ms = float(tt.item())
+        e_ms = max_over_ranks(a.elapsed_time(b), world)
         h2d = sum(t.numel() * t.element_size() for t in (h_ids, h_X, h_W, h_G))
         d2h = sum(t.numel() * t.element_size() for t in (h_dprob, h_fp, h_fps))
-        e2e = {"value": world * flops * args.e2e_steps / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e2e = {"value": whole_job_tflops(flops, args.e2e_steps, world, e_ms), "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": e_ms / args.e2e_steps}
 

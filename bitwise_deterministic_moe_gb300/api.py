@@ -41,7 +41,10 @@ class DmoeError(RuntimeError):
 
 
 class _Launch(ctypes.Structure):
-    _fields_ = [("num_ctas", ctypes.c_int), ("reserved", ctypes.c_int)]
+    _fields_ = [("num_ctas", ctypes.c_int), ("flags", ctypes.c_int)]
+
+
+LAUNCH_TEST_STALL = 1
 
 
 _lib = None
@@ -109,8 +112,8 @@ def _need(t: torch.Tensor, dtype, name: str, shape=None):
         raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
 
 
-def _launch(num_ctas: int):
-    return ctypes.byref(_Launch(int(num_ctas), 0))
+def _launch(num_ctas: int, flags: int = 0):
+    return ctypes.byref(_Launch(int(num_ctas), int(flags)))
 
 
 # ------------------------------------------------------------------ workspace
@@ -174,7 +177,7 @@ def grouped_gemm_fwd(X_perm, W, expert_offsets, ws, out=None, num_ctas: int = 0,
 
 
 def grouped_gemm_dprob(X_perm, W, expert_offsets, grad_out, row_src, topk: int, ws, out=None, slots=None,
-                       dprob=None, num_ctas: int = 0, stream=None):
+                       dprob=None, num_ctas: int = 0, stream=None, flags: int = 0):
     """Deterministic path: returns (expert_out bf16 [R,N], dprob fp32 [T,topk], slots fp32 [S,R])."""
     R, E, K, N = _gemm_shapes(X_perm, W, expert_offsets)
     T = R // topk
@@ -193,7 +196,7 @@ def grouped_gemm_dprob(X_perm, W, expert_offsets, grad_out, row_src, topk: int, 
     _need(dprob, torch.float32, "dprob", (T, topk))
     st = load().moe_grouped_gemm_dprob(_ptr(X_perm), _ptr(W), _ptr(expert_offsets), R, E, K, N, _ptr(out),
                                        _ptr(grad_out), _ptr(row_src), T, topk, _ptr(slots), _ptr(dprob),
-                                       _launch(num_ctas), _ptr(ws), ws.numel(), _stream(stream))
+                                       _launch(num_ctas, flags), _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "moe_grouped_gemm_dprob")
     return out, dprob, slots
 

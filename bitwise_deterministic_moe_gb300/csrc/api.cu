@@ -151,6 +151,7 @@ dmoe_status moe_grouped_gemm_fwd(const void* X_perm, const void* W, const int32_
   a.status = status_ptr(ws);
   a.sched = sched_ptr(ws);
   a.num_ctas = launch ? launch->num_ctas : 0;
+  a.flags = launch ? launch->flags : 0;
   if (a.num_ctas < 0) return DMOE_ERR_INVALID_ARG;
   return cuda_status(launch_grouped_gemm(GemmMode::kFwd, a, reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -181,6 +182,7 @@ dmoe_status moe_grouped_gemm_dprob(const void* X_perm, const void* W, const int3
   a.status = status_ptr(ws);
   a.sched = sched_ptr(ws);
   a.num_ctas = launch ? launch->num_ctas : 0;
+  a.flags = launch ? launch->flags : 0;
   if (a.num_ctas < 0) return DMOE_ERR_INVALID_ARG;
   cudaError_t e = launch_grouped_gemm(GemmMode::kSlots, a, s);
   if (e != cudaSuccess) return DMOE_ERR_CUDA;
@@ -211,6 +213,7 @@ dmoe_status moe_grouped_gemm_dprob_atomic(const void* X_perm, const void* W, con
   a.status = status_ptr(ws);
   a.sched = sched_ptr(ws);
   a.num_ctas = launch ? launch->num_ctas : 0;
+  a.flags = launch ? launch->flags : 0;
   if (a.num_ctas < 0) return DMOE_ERR_INVALID_ARG;
   return cuda_status(launch_grouped_gemm(GemmMode::kAtomic, a, s));
 }

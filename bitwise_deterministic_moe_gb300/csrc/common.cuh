@@ -10,9 +10,9 @@
 
 namespace dmoe {
 
-// Wall-clock limit of every spin-wait on the device.  A healthy pipeline
-// waits microseconds; hitting this limit means a broken invariant, and the
-// kernel then records DMOE_ERR_TIMEOUT and unwinds instead of hanging.
+// Default wall-clock limit of every spin-wait on the device.  A healthy
+// pipeline waits microseconds; hitting the limit means a broken invariant,
+// and the kernel then records DMOE_ERR_TIMEOUT and unwinds instead of hanging.
 constexpr unsigned long long kWaitLimitNs = 2000ull * 1000ull * 1000ull;  // 2 s
 
 __device__ __forceinline__ void record_error(int* status, int code) {
@@ -51,17 +51,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase with the given parity to complete.  Gives up
-// (returns false) when *abort is set by another role or after kWaitLimitNs,
+// (returns false) when *abort is set by another role or after limit_ns,
 // recording DMOE_ERR_TIMEOUT and raising *abort in the latter case.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          int* status) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, int* status,
+                                          unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   unsigned long long t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*abort) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         record_error(status, DMOE_ERR_TIMEOUT);
         *abort = 1;
         return false;
@@ -73,9 +73,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 // Warp-uniform variant: lane 0 waits, the outcome is broadcast, and the
 // __syncwarp orders the other lanes' later reads after the completed phase.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort, int* status,
-                                          int lane) {
+                                          int lane, unsigned long long limit_ns) {
   int ok = 1;
-  if (lane == 0) ok = mbar_wait(bar, parity, abort, status) ? 1 : 0;
+  if (lane == 0) ok = mbar_wait(bar, parity, abort, status, limit_ns) ? 1 : 0;
   ok = __shfl_sync(0xffffffffu, ok, 0);
   __syncwarp();
   return ok != 0;
@@ -83,10 +83,10 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 
 // Same, with its own (shorter) limit and no abort flag: used on the unwind
 // path to let copies already in flight land before the CTA exits.
-__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
   unsigned long long t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > kWaitLimitNs / 4) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   }
   return true;
 }

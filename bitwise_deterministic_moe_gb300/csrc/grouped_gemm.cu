@@ -83,6 +83,8 @@ struct KParams {
   float* dprob;
   int* status;
   int* sched;   // [0] next-tile counter, [1] finished-CTA counter; zero between launches
+  unsigned long long wait_ns;   // limit of every pipeline wait
+  int stall_test;               // test only: CTA 0 arms its first stage but never loads it
 };
 
 // Shared-memory matrix descriptor for a K-major operand tile written by TMA
@@ -235,7 +237,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
       int tile = blockIdx.x;
       for (int qi = 0;; ++qi) {
         const int qs = qi % TQ;
-        if (!mbar_wait(smem_u32(&c.tq_empty[qs]), uint32_t((qi / TQ) & 1) ^ 1u, &c.abort, p.status)) break;
+        if (!mbar_wait(smem_u32(&c.tq_empty[qs]), uint32_t((qi / TQ) & 1) ^ 1u, &c.abort, p.status, p.wait_ns)) break;
         const int cur = tile < total_tiles ? tile : -1;
         c.tq_tile[qs] = cur;
         mbar_arrive(smem_u32(&c.tq_full[qs]));
@@ -245,20 +247,25 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
         const int brow = tl.e * p.N + tl.n0;
         bool ok = true;
         for (int kb = 0; kb < p.KB; ++kb) {
-          if (!mbar_wait(smem_u32(&c.empty[stage]), ph ^ 1u, &c.abort, p.status)) { ok = false; break; }
+          if (!mbar_wait(smem_u32(&c.empty[stage]), ph ^ 1u, &c.abort, p.status, p.wait_ns)) { ok = false; break; }
           const uint32_t full = smem_u32(&c.full[stage]);
           const uint32_t sa = stage0 + stage * STAGE_BYTES;
           mbar_arrive_expect_tx(full, STAGE_BYTES);
-          tma_load_2d(sa, &tmap_a, full, kb * BK, tl.row0);
-          tma_load_2d(sa + A_STAGE_BYTES, &tmap_b, full, kb * BK, brow);
-          ++issued[stage];
+          if (p.stall_test && blockIdx.x == 0 && qi == 0 && kb == 0) {
+            // expected bytes that never arrive: the MMA's wait on this stage
+            // must run out and report DMOE_ERR_TIMEOUT (nothing is in flight)
+          } else {
+            tma_load_2d(sa, &tmap_a, full, kb * BK, tl.row0);
+            tma_load_2d(sa + A_STAGE_BYTES, &tmap_b, full, kb * BK, brow);
+            ++issued[stage];
+          }
           if (++stage == STAGES) { stage = 0; ph ^= 1u; }
         }
         if (!ok) break;
       }
       // let every copy this thread started land before the CTA can exit
       for (int s = 0; s < STAGES; ++s)
-        if (issued[s] > 0) mbar_wait_drain(smem_u32(&c.full[s]), uint32_t(issued[s] - 1) & 1u);
+        if (issued[s] > 0) mbar_wait_drain(smem_u32(&c.full[s]), uint32_t(issued[s] - 1) & 1u, p.wait_ns / 4);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -269,16 +276,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
       uint32_t aph = 0;
       for (int qi = 0;; ++qi) {
         const int qs = qi % TQ;
-        if (!mbar_wait(smem_u32(&c.tq_full[qs]), uint32_t((qi / TQ) & 1), &c.abort, p.status)) break;
+        if (!mbar_wait(smem_u32(&c.tq_full[qs]), uint32_t((qi / TQ) & 1), &c.abort, p.status, p.wait_ns)) break;
         const int cur = c.tq_tile[qs];
         mbar_arrive(smem_u32(&c.tq_empty[qs]));
         if (cur < 0) break;
-        if (!mbar_wait(smem_u32(&c.acc_empty[acc]), aph ^ 1u, &c.abort, p.status)) break;
+        if (!mbar_wait(smem_u32(&c.acc_empty[acc]), aph ^ 1u, &c.abort, p.status, p.wait_ns)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
         bool ok = true;
         for (int kb = 0; kb < p.KB; ++kb) {
-          if (!mbar_wait(smem_u32(&c.full[stage]), ph, &c.abort, p.status)) { ok = false; break; }
+          if (!mbar_wait(smem_u32(&c.full[stage]), ph, &c.abort, p.status, p.wait_ns)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = stage0 + stage * STAGE_BYTES;
           const uint64_t adesc = smem_desc_k128(sa);
@@ -298,7 +305,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
       }
       // every MMA must be finished before tensor memory is released
       tc_commit(smem_u32(&c.mma_done));
-      mbar_wait_drain(smem_u32(&c.mma_done), 0);
+      mbar_wait_drain(smem_u32(&c.mma_done), 0, p.wait_ns / 4);
     }
   } else {
     // -------------------------------------------------- epilogue (8 warps)
@@ -319,7 +326,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
     uint32_t aph = 0;
     for (int qi = 0;; ++qi) {
       const int qs = qi % TQ;
-      if (!warp_wait(smem_u32(&c.tq_full[qs]), uint32_t((qi / TQ) & 1), &c.abort, p.status, lane)) break;
+      if (!warp_wait(smem_u32(&c.tq_full[qs]), uint32_t((qi / TQ) & 1), &c.abort, p.status, lane, p.wait_ns)) break;
       const int cur = c.tq_tile[qs];
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&c.tq_empty[qs]));
@@ -356,7 +363,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
           for (int ch = 0; ch < 4; ++ch) g[ch * 4 + i] = ok[i] ? ldg_nc_v4_hint(gp + ch * 32, pol_keep) : make_uint4(0, 0, 0, 0);
         }
       }
-      if (!warp_wait(smem_u32(&c.acc_full[acc]), aph, &c.abort, p.status, lane)) break;
+      if (!warp_wait(smem_u32(&c.acc_full[acc]), aph, &c.abort, p.status, lane, p.wait_ns)) break;
       tc_fence_after();
       if (active) {
         const uint32_t tcol = tmem_base + uint32_t(acc * BN + h * SLOT) + (uint32_t(q * 32) << 16);
@@ -502,6 +509,8 @@ cudaError_t launch_grouped_gemm(GemmMode mode, const GemmArgs& a, cudaStream_t s
   kp.status = a.status;
   kp.sched = a.sched;
   if (!kp.sched) return cudaErrorInvalidValue;
+  kp.stall_test = (a.flags & DMOE_LAUNCH_TEST_STALL) ? 1 : 0;
+  kp.wait_ns = kp.stall_test ? 200ull * 1000ull * 1000ull : kWaitLimitNs;   // a short limit for the test
   int grid = a.num_ctas > 0 ? a.num_ctas : device_sm_count();
   switch (mode) {
     case GemmMode::kFwd: return launch_mode<int(GemmMode::kFwd)>(ta, tb, kp, grid, stream);

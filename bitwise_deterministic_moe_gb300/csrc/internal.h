@@ -25,6 +25,7 @@ struct GemmArgs {
   int* status;                // device status word (may be null: errors not recorded)
   int* sched;                 // 2 device ints, zero between launches: dynamic tile counter
   int num_ctas;               // 0 = one per SM
+  int flags;                  // dmoe_launch.flags
 };
 
 cudaError_t launch_grouped_gemm(GemmMode mode, const GemmArgs& a, cudaStream_t stream);

@@ -95,6 +95,7 @@ extern "C" dmoe_status moe_grouped_gemm_dprob_noalloc(const void* X_perm, const 
   a.status = nullptr;   // no caller workspace: device-side errors are not recorded
   a.sched = sched;
   a.num_ctas = launch ? launch->num_ctas : 0;
+  a.flags = launch ? launch->flags : 0;
   if (launch_grouped_gemm(GemmMode::kSlots, a, s) != cudaSuccess) return DMOE_ERR_CUDA;
   if (launch_dprob_combine(slots, row_src, R, S, dprob, s) != cudaSuccess) return DMOE_ERR_CUDA;
   return DMOE_OK;

@@ -65,11 +65,17 @@ typedef enum dmoe_dtype {
 } dmoe_dtype;
 
 /* Launch options of the grouped GEMM.  num_ctas = persistent CTAs (0 = one
- * per SM).  Any value gives the same bits. */
+ * per SM); any value gives the same bits.  flags: 0, or
+ * DMOE_LAUNCH_TEST_STALL to exercise the failure path: the first CTA arms
+ * one pipeline stage but never loads it, so the wait on it runs out (after a
+ * 200 ms limit instead of the usual 2 s), the kernel records
+ * DMOE_ERR_TIMEOUT, unwinds and frees its tensor memory; outputs are then
+ * undefined and the context stays usable. */
 typedef struct dmoe_launch {
     int num_ctas;
-    int reserved;
+    int flags;
 } dmoe_launch;
+#define DMOE_LAUNCH_TEST_STALL 1
 
 /* Supported shapes of the grouped GEMM calls:
  *   1 <= E <= DMOE_MAX_EXPERTS, 8 <= K <= 65536 with K % 8 == 0,
