@@ -45,6 +45,8 @@ class _Launch(ctypes.Structure):
 
 
 LAUNCH_TEST_STALL = 1
+LAUNCH_SINGLE_CTA = 2   # force the one-SM-per-tile kernel
+LAUNCH_CTA_PAIRS = 4    # force the 2-SM (CTA pair) kernel
 
 
 _lib = None
@@ -165,13 +167,13 @@ def _gemm_shapes(X, W, offs):
     return R, E, K, N
 
 
-def grouped_gemm_fwd(X_perm, W, expert_offsets, ws, out=None, num_ctas: int = 0, stream=None):
+def grouped_gemm_fwd(X_perm, W, expert_offsets, ws, out=None, num_ctas: int = 0, stream=None, flags: int = 0):
     R, E, K, N = _gemm_shapes(X_perm, W, expert_offsets)
     if out is None:
         out = torch.empty(R, N, dtype=torch.bfloat16, device=X_perm.device)
     _need(out, torch.bfloat16, "expert_out", (R, N))
     st = load().moe_grouped_gemm_fwd(_ptr(X_perm), _ptr(W), _ptr(expert_offsets), R, E, K, N, _ptr(out),
-                                     _launch(num_ctas), _ptr(ws), ws.numel(), _stream(stream))
+                                     _launch(num_ctas, flags), _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "moe_grouped_gemm_fwd")
     return out
 
@@ -202,7 +204,7 @@ def grouped_gemm_dprob(X_perm, W, expert_offsets, grad_out, row_src, topk: int, 
 
 
 def grouped_gemm_dprob_atomic(X_perm, W, expert_offsets, grad_out, row_src, topk: int, ws, out=None, dprob=None,
-                              num_ctas: int = 0, stream=None):
+                              num_ctas: int = 0, stream=None, flags: int = 0):
     """Nondeterministic atomicAdd control: returns (expert_out, dprob)."""
     R, E, K, N = _gemm_shapes(X_perm, W, expert_offsets)
     T = R // topk
@@ -217,7 +219,7 @@ def grouped_gemm_dprob_atomic(X_perm, W, expert_offsets, grad_out, row_src, topk
     _need(dprob, torch.float32, "dprob", (T, topk))
     st = load().moe_grouped_gemm_dprob_atomic(_ptr(X_perm), _ptr(W), _ptr(expert_offsets), R, E, K, N, _ptr(out),
                                               _ptr(grad_out), _ptr(row_src), T, topk, _ptr(dprob),
-                                              _launch(num_ctas), _ptr(ws), ws.numel(), _stream(stream))
+                                              _launch(num_ctas, flags), _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "moe_grouped_gemm_dprob_atomic")
     return out, dprob
 

@@ -19,7 +19,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libdmoe.so")
-SOURCES = ["api.cu", "grouped_gemm.cu", "routing.cu", "dprob.cu", "fingerprint.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "grouped_gemm.cu", "grouped_gemm_2sm.cu", "routing.cu", "dprob.cu", "fingerprint.cu",
+           "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

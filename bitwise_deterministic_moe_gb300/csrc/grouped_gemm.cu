@@ -225,9 +225,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------ TMA producer
-      int issued[STAGES];
-#pragma unroll
-      for (int s = 0; s < STAGES; ++s) issued[s] = 0;
+      // stages are used round-robin, so stage s has been loaded
+      // (issued_total - s + STAGES - 1) / STAGES times (minus the one skipped
+      // by the stall test); no per-stage array in local memory
+      int issued_total = 0;
+      bool skipped_first = false;
       int stage = 0;
       uint32_t ph = 0;
       // Tiles are handed out dynamically (first tile = blockIdx.x, then a
@@ -254,18 +256,22 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
           if (p.stall_test && blockIdx.x == 0 && qi == 0 && kb == 0) {
             // expected bytes that never arrive: the MMA's wait on this stage
             // must run out and report DMOE_ERR_TIMEOUT (nothing is in flight)
+            skipped_first = true;
           } else {
             tma_load_2d(sa, &tmap_a, full, kb * BK, tl.row0);
             tma_load_2d(sa + A_STAGE_BYTES, &tmap_b, full, kb * BK, brow);
-            ++issued[stage];
           }
+          ++issued_total;
           if (++stage == STAGES) { stage = 0; ph ^= 1u; }
         }
         if (!ok) break;
       }
       // let every copy this thread started land before the CTA can exit
-      for (int s = 0; s < STAGES; ++s)
-        if (issued[s] > 0) mbar_wait_drain(smem_u32(&c.full[s]), uint32_t(issued[s] - 1) & 1u, p.wait_ns / 4);
+      for (int s = 0; s < STAGES; ++s) {
+        const int n = (issued_total - s + STAGES - 1) / STAGES - ((s == 0 && skipped_first) ? 1 : 0);
+        if (n > 0 && !(s == 0 && skipped_first))
+          mbar_wait_drain(smem_u32(&c.full[s]), uint32_t(n - 1) & 1u, p.wait_ns / 4);
+      }
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -457,8 +463,10 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+}  // namespace
+
 // 2-D bf16 tensor [rows, cols] (cols contiguous), box [box_rows, 64], 128-byte swizzle.
-bool make_tmap(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+bool make_tmap_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {cols, rows};
@@ -470,6 +478,8 @@ bool make_tmap(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, ui
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
+
+namespace {
 
 template <int MODE>
 cudaError_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const KParams& kp, int grid,
@@ -487,11 +497,11 @@ cudaError_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const KPar
 
 }  // namespace
 
-cudaError_t launch_grouped_gemm(GemmMode mode, const GemmArgs& a, cudaStream_t stream) {
+cudaError_t launch_grouped_gemm_1sm(GemmMode mode, const GemmArgs& a, cudaStream_t stream) {
   if (a.R == 0) return cudaSuccess;
   CUtensorMap ta, tb;
-  if (!make_tmap(&ta, a.X, uint64_t(a.R), uint64_t(a.K), BM)) return cudaErrorInvalidValue;
-  if (!make_tmap(&tb, a.W, uint64_t(a.E) * a.N, uint64_t(a.K), BN)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&ta, a.X, uint64_t(a.R), uint64_t(a.K), BM)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&tb, a.W, uint64_t(a.E) * a.N, uint64_t(a.K), BN)) return cudaErrorInvalidValue;
   KParams kp;
   kp.offsets = a.offsets;
   kp.E = a.E;

@@ -28,7 +28,8 @@ struct GemmArgs {
   int flags;                  // dmoe_launch.flags
 };
 
-cudaError_t launch_grouped_gemm(GemmMode mode, const GemmArgs& a, cudaStream_t stream);
+cudaError_t launch_grouped_gemm(GemmMode mode, const GemmArgs& a, cudaStream_t stream);       // CTA pairs
+cudaError_t launch_grouped_gemm_1sm(GemmMode mode, const GemmArgs& a, cudaStream_t stream);   // single CTAs
 
 // routing
 size_t routing_scratch_bytes(long long R, int E);

@@ -64,18 +64,27 @@ typedef enum dmoe_dtype {
     DMOE_U16 = 10, DMOE_U32 = 11, DMOE_U64 = 12
 } dmoe_dtype;
 
-/* Launch options of the grouped GEMM.  num_ctas = persistent CTAs (0 = one
- * per SM); any value gives the same bits.  flags: 0, or
- * DMOE_LAUNCH_TEST_STALL to exercise the failure path: the first CTA arms
- * one pipeline stage but never loads it, so the wait on it runs out (after a
- * 200 ms limit instead of the usual 2 s), the kernel records
- * DMOE_ERR_TIMEOUT, unwinds and frees its tensor memory; outputs are then
- * undefined and the context stays usable. */
+/* Launch options of the grouped GEMM.  num_ctas = persistent CTAs (0 = as
+ * many as can be resident); any value gives the same bits.  Two kernels
+ * implement every call and give bitwise identical results: one SM per
+ * 128x256 tile, or CTA pairs (2-SM tensor-core MMA) per 256x256 tile, chosen
+ * by default from the mean rows per expert (pairs when R >= 512*E).  On the
+ * pair kernel an odd num_ctas is rounded down to even (minimum 2) and capped
+ * at the resident count.  flags, OR-ed:
+ *   DMOE_LAUNCH_SINGLE_CTA  force the single-CTA kernel
+ *   DMOE_LAUNCH_CTA_PAIRS   force the CTA-pair kernel
+ *   DMOE_LAUNCH_TEST_STALL  exercise the failure path: the first CTA arms one
+ *     pipeline stage but never loads it, so the wait on it runs out (after a
+ *     200 ms limit instead of the usual 2 s), the kernel records
+ *     DMOE_ERR_TIMEOUT, unwinds and frees its tensor memory; outputs are
+ *     then undefined and the context stays usable. */
 typedef struct dmoe_launch {
     int num_ctas;
     int flags;
 } dmoe_launch;
 #define DMOE_LAUNCH_TEST_STALL 1
+#define DMOE_LAUNCH_SINGLE_CTA 2
+#define DMOE_LAUNCH_CTA_PAIRS 4
 
 /* Supported shapes of the grouped GEMM calls:
  *   1 <= E <= DMOE_MAX_EXPERTS, 8 <= K <= 65536 with K % 8 == 0,

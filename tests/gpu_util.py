@@ -38,10 +38,11 @@ class Problem:
         self.ws = api.workspace(cfg.T, cfg.topk, cfg.E, dev)
         self.off, self.src = api.permute_indices(self.ids, cfg.E, self.ws)
 
-    def run_dprob(self, num_ctas=0, stream=None, out=None, slots=None, dprob=None, ws=None):
+    def run_dprob(self, num_ctas=0, stream=None, out=None, slots=None, dprob=None, ws=None, flags=0):
         return api.grouped_gemm_dprob(self.X, self.W, self.off, self.G, self.src, self.cfg.topk,
                                       self.ws if ws is None else ws,
-                                      out=out, slots=slots, dprob=dprob, num_ctas=num_ctas, stream=stream)
+                                      out=out, slots=slots, dprob=dprob, num_ctas=num_ctas, stream=stream,
+                                      flags=flags)
 
 
 def check_rows_against_oracle(prob, out, slots, dprob, rows):

@@ -29,20 +29,23 @@ def same(a, b):
     return all(torch.equal(x[0], y[0]) and x[1] == y[1] for x, y in zip(a, b))
 
 
-def test_repeat_grids_streams_small():
+@pytest.mark.parametrize("flags", [api.LAUNCH_SINGLE_CTA, api.LAUNCH_CTA_PAIRS], ids=["single", "pairs"])
+def test_repeat_grids_streams_small(flags):
     cfg = synth.CONFIGS["small"]
     prob = Problem(cfg)
-    out, dprob, slots = prob.run_dprob()
+    out, dprob, slots = prob.run_dprob(flags=flags)
     ref = fps(out, slots, dprob)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     for grid in (sms, sms // 2, 37, 1):
         for _ in range(3):
-            o, d, s = prob.run_dprob(num_ctas=grid)
+            o, d, s = prob.run_dprob(num_ctas=grid, flags=flags)
             assert same(fps(o, s, d), ref), grid
     assert api.read_status(prob.ws) == 0
 
 
 def test_stress_100_launches_3_grids_2_streams():
+    """Default kernel choice (CTA pairs for this shape) and, every tenth
+    round, the single-CTA kernel: all outputs match the first run's bits."""
     cfg = synth.CONFIGS["stress"]
     prob = Problem(cfg)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
@@ -56,9 +59,10 @@ def test_stress_100_launches_3_grids_2_streams():
     launches = 0
     for it in range(100 // 2):
         for grid in (sms, sms // 2, 37):
+            flags = api.LAUNCH_SINGLE_CTA if it % 10 == 5 else 0
             for s, (o, d, sl), w in zip(streams, bufs, wss):
                 with torch.cuda.stream(s):
-                    prob.run_dprob(num_ctas=grid, out=o, slots=sl, dprob=d, stream=s, ws=w)
+                    prob.run_dprob(num_ctas=grid, out=o, slots=sl, dprob=d, stream=s, ws=w, flags=flags)
                 launches += 1
             if it % 10 == 0 or it == 100 // 2 - 1:
                 torch.cuda.synchronize()

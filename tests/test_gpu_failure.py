@@ -23,16 +23,17 @@ def bits(t):
     return t.view(torch.int16 if t.element_size() == 2 else torch.int32).clone()
 
 
-def test_wait_limit_reports_timeout_and_context_survives():
+@pytest.mark.parametrize("kernel", [api.LAUNCH_SINGLE_CTA, api.LAUNCH_CTA_PAIRS], ids=["single", "pairs"])
+def test_wait_limit_reports_timeout_and_context_survives(kernel):
     prob = Problem(synth.CONFIGS["small"])
-    out, dprob, _ = prob.run_dprob()
+    out, dprob, _ = prob.run_dprob(flags=kernel)
     ref_out, ref_dp = bits(out), bits(dprob)
     assert api.read_status(prob.ws) == 0
     api.grouped_gemm_dprob(prob.X, prob.W, prob.off, prob.G, prob.src, prob.cfg.topk, prob.ws,
-                           flags=api.LAUNCH_TEST_STALL)
+                           flags=api.LAUNCH_TEST_STALL | kernel)
     assert api.read_status(prob.ws) == 4          # DMOE_ERR_TIMEOUT
     for _ in range(2):                             # the context and the workspace still work
-        out2, dprob2, _ = prob.run_dprob()
+        out2, dprob2, _ = prob.run_dprob(flags=kernel)
         assert api.read_status(prob.ws) == 0
         assert torch.equal(bits(out2), ref_out)
         assert torch.equal(bits(dprob2), ref_dp)

@@ -28,20 +28,26 @@ SHAPES = [
 ]
 
 
+KERNELS = [api.LAUNCH_SINGLE_CTA, api.LAUNCH_CTA_PAIRS]
+KERNEL_IDS = ["single", "pairs"]
+
+
+@pytest.mark.parametrize("flags", KERNELS, ids=KERNEL_IDS)
 @pytest.mark.parametrize("cfg", SHAPES, ids=[c.name for c in SHAPES])
-def test_full_parity_small_shapes(cfg):
+def test_full_parity_small_shapes(cfg, flags):
     prob = Problem(cfg)
-    out, dprob, slots = prob.run_dprob()
+    out, dprob, slots = prob.run_dprob(flags=flags)
     assert api.read_status(prob.ws) == 0
     rows = np.arange(cfg.R)
     gpu_util.check_rows_against_oracle(prob, out, slots, dprob, rows)
 
 
+@pytest.mark.parametrize("flags", KERNELS, ids=KERNEL_IDS)
 @pytest.mark.parametrize("cfg", SHAPES[:2], ids=[c.name for c in SHAPES[:2]])
-def test_fwd_equals_dprob_output_and_unfused_epilogue(cfg):
+def test_fwd_equals_dprob_output_and_unfused_epilogue(cfg, flags):
     prob = Problem(cfg)
-    out, dprob, slots = prob.run_dprob()
-    out2 = api.grouped_gemm_fwd(prob.X, prob.W, prob.off, prob.ws)
+    out, dprob, slots = prob.run_dprob(flags=flags)
+    out2 = api.grouped_gemm_fwd(prob.X, prob.W, prob.off, prob.ws, flags=flags)
     assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
     slots2 = api.dprob_epilogue(prob.G, out, prob.off, prob.src, cfg.topk)
     assert torch.equal(slots.view(torch.int32), slots2.view(torch.int32))      # fused == unfused, bitwise
@@ -68,11 +74,13 @@ def test_unfused_epilogue_on_oracle_output():
     assert np.abs(dprob.double().cpu().numpy() - D).max() <= 2e-3 * np.abs(D).max()
 
 
-def test_atomic_control_close_to_deterministic():
+@pytest.mark.parametrize("flags", KERNELS, ids=KERNEL_IDS)
+def test_atomic_control_close_to_deterministic(flags):
     cfg = SHAPES[4]
     prob = Problem(cfg)
-    out, dprob, _ = prob.run_dprob()
-    out_a, dprob_a = api.grouped_gemm_dprob_atomic(prob.X, prob.W, prob.off, prob.G, prob.src, cfg.topk, prob.ws)
+    out, dprob, _ = prob.run_dprob(flags=flags)
+    out_a, dprob_a = api.grouped_gemm_dprob_atomic(prob.X, prob.W, prob.off, prob.G, prob.src, cfg.topk, prob.ws,
+                                                   flags=flags)
     assert torch.equal(out.view(torch.int16), out_a.view(torch.int16))
     scale = dprob.abs().max().item()
     assert (dprob - dprob_a).abs().max().item() <= 1e-5 * scale
@@ -80,28 +88,30 @@ def test_atomic_control_close_to_deterministic():
     gpu_util.check_rows_against_oracle(prob, out_a, None, dprob_a, rows)
 
 
-def test_empty_experts_and_hot_expert():
+@pytest.mark.parametrize("flags", KERNELS, ids=KERNEL_IDS)
+def test_empty_experts_and_hot_expert(flags):
     cfg = synth.custom_config("holes", T=900, E=40, topk=4, K=192, N=256, index=305)
     inp = synth.make_inputs(cfg)
     ids = inp.topk_ids.copy()
     ids[ids % 5 == 0] = 1           # experts 0,5,10,... empty; expert 1 hot (duplicates allowed)
     inp2 = synth.MoEInputs(cfg, ids, inp.X, inp.W, inp.G, inp.probs)
     prob = Problem(cfg, inp2)
-    out, dprob, slots = prob.run_dprob()
+    out, dprob, slots = prob.run_dprob(flags=flags)
     assert api.read_status(prob.ws) == 0
     gpu_util.check_rows_against_oracle(prob, out, slots, dprob, np.arange(cfg.R))
 
 
-def test_bad_offsets_set_routing_status():
+@pytest.mark.parametrize("flags", KERNELS, ids=KERNEL_IDS)
+def test_bad_offsets_set_routing_status(flags):
     cfg = SHAPES[0]
     prob = Problem(cfg)
     bad = prob.off.clone()
     bad[3] = bad[4] + 1            # not monotone
-    api.grouped_gemm_fwd(prob.X, prob.W, bad, prob.ws)
+    api.grouped_gemm_fwd(prob.X, prob.W, bad, prob.ws, flags=flags)
     assert api.read_status(prob.ws) == 3
     bad = prob.off.clone()
     bad[-1] -= 1                   # does not end at R
-    api.grouped_gemm_fwd(prob.X, prob.W, bad, prob.ws)
+    api.grouped_gemm_fwd(prob.X, prob.W, bad, prob.ws, flags=flags)
     assert api.read_status(prob.ws) == 3
     assert api.read_status(prob.ws) == 0   # cleared by the read
 
@@ -116,14 +126,29 @@ def test_zero_rows():
     assert out.shape == (0, 256)
 
 
-@pytest.mark.parametrize("name", ["small", "latent"])
-def test_full_size_sampled_rows(name):
-    """The benchmark's configuration (one CTA per SM) at full size, on sampled
-    rows the oracle computes one by one."""
+@pytest.mark.parametrize("flags", [0] + KERNELS, ids=["default"] + KERNEL_IDS)
+@pytest.mark.parametrize("name", ["small", "latent", "imbal"])
+def test_full_size_sampled_rows(name, flags):
+    """Full size, in the benchmark's launch configuration (flags 0) and with
+    each kernel forced, on sampled rows the oracle computes one by one."""
     cfg = synth.CONFIGS[name]
     prob = Problem(cfg)
-    out, dprob, slots = prob.run_dprob()
+    out, dprob, slots = prob.run_dprob(flags=flags)
     assert api.read_status(prob.ws) == 0
     off = prob.off.cpu().numpy()
     rows = gpu_util.sample_rows(off, 96, seed=cfg.seed)
     gpu_util.check_rows_against_oracle(prob, out, slots, dprob, rows)
+
+
+@pytest.mark.parametrize("name", ["tiny", "small", "latent", "imbal"])
+def test_single_and_pair_kernels_bitwise_equal(name):
+    """The two kernels give the same bits, so the automatic choice between
+    them never changes a result."""
+    prob = Problem(synth.CONFIGS[name])
+    o1, d1, s1 = prob.run_dprob(flags=api.LAUNCH_SINGLE_CTA)
+    o1, d1, s1 = o1.clone(), d1.clone(), s1.clone()
+    o2, d2, s2 = prob.run_dprob(flags=api.LAUNCH_CTA_PAIRS)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(s1.view(torch.int32), s2.view(torch.int32))
+    assert torch.equal(d1.view(torch.int32), d2.view(torch.int32))
+    assert api.read_status(prob.ws) == 0
