@@ -18,6 +18,7 @@ __global__ void __launch_bounds__(256)
 dprob_epilogue_kernel(const uint16_t* __restrict__ grad_out, const uint16_t* __restrict__ expert_out,
                       const int32_t* __restrict__ offsets, const int32_t* __restrict__ row_src, int R, int E,
                       int topk, int N, int S, float* __restrict__ slots, int* status) {
+  pdl_begin();
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= (long long)R * S) return;
   const int s = int(idx / R);
@@ -55,6 +56,7 @@ template <int S_STATIC>
 __global__ void __launch_bounds__(256)
 dprob_combine_kernel(const float* __restrict__ slots, const int32_t* __restrict__ row_src, int R, int S,
                      float* __restrict__ dprob) {
+  pdl_begin();
   const int r = blockIdx.x * blockDim.x + threadIdx.x;
   if (r >= R) return;
   const int nS = S_STATIC > 0 ? S_STATIC : S;
@@ -83,10 +85,9 @@ cudaError_t launch_dprob_epilogue(const void* grad_out, const void* expert_out, 
   const long long total = (long long)R * S;
   if (total == 0) return cudaSuccess;
   const unsigned grid = unsigned((total + 255) / 256);
-  dprob_epilogue_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(grad_out),
-                                                  static_cast<const uint16_t*>(expert_out), offsets, row_src, R, E,
-                                                  topk, N, S, slots, status);
-  return cudaGetLastError();
+  return launch_chained(dprob_epilogue_kernel, dim3(grid), dim3(256), 0, stream,
+                        static_cast<const uint16_t*>(grad_out), static_cast<const uint16_t*>(expert_out), offsets,
+                        row_src, R, E, topk, N, S, slots, status);
 }
 
 cudaError_t launch_dprob_combine(const float* slots, const int32_t* row_src, int R, int S, float* dprob,
@@ -94,12 +95,11 @@ cudaError_t launch_dprob_combine(const float* slots, const int32_t* row_src, int
   if (R == 0) return cudaSuccess;
   const unsigned grid = unsigned((R + 255) / 256);
   switch (S) {
-    case 1: dprob_combine_kernel<1><<<grid, 256, 0, stream>>>(slots, row_src, R, S, dprob); break;
-    case 2: dprob_combine_kernel<2><<<grid, 256, 0, stream>>>(slots, row_src, R, S, dprob); break;
-    case 16: dprob_combine_kernel<16><<<grid, 256, 0, stream>>>(slots, row_src, R, S, dprob); break;
-    default: dprob_combine_kernel<0><<<grid, 256, 0, stream>>>(slots, row_src, R, S, dprob); break;
+    case 1: return launch_chained(dprob_combine_kernel<1>, dim3(grid), dim3(256), 0, stream, slots, row_src, R, S, dprob);
+    case 2: return launch_chained(dprob_combine_kernel<2>, dim3(grid), dim3(256), 0, stream, slots, row_src, R, S, dprob);
+    case 16: return launch_chained(dprob_combine_kernel<16>, dim3(grid), dim3(256), 0, stream, slots, row_src, R, S, dprob);
+    default: return launch_chained(dprob_combine_kernel<0>, dim3(grid), dim3(256), 0, stream, slots, row_src, R, S, dprob);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace dmoe

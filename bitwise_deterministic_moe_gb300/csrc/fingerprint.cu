@@ -82,6 +82,7 @@ template <bool VEC>
 __global__ void __launch_bounds__(kThreads)
 fp_positional_kernel(const uint8_t* __restrict__ data, size_t nbytes, size_t chunk_bytes, unsigned parts,
                      unsigned long long* __restrict__ acc) {
+  pdl_begin();
   const size_t c = blockIdx.x / parts;
   const size_t b0 = c * chunk_bytes + size_t(blockIdx.x % parts) * kPartBytes;
   const size_t chunk_end = min(nbytes, (c + 1) * chunk_bytes);
@@ -121,6 +122,7 @@ fp_positional_kernel(const uint8_t* __restrict__ data, size_t nbytes, size_t chu
 
 __global__ void fp_finalize_kernel(unsigned long long* __restrict__ acc, size_t nchunks, size_t nbytes,
                                    size_t chunk_bytes) {
+  pdl_begin();
   const size_t c = size_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (c >= nchunks) return;
   const size_t len = min(chunk_bytes, nbytes - c * chunk_bytes);
@@ -153,6 +155,7 @@ template <int ES>
 __global__ void __launch_bounds__(kThreads)
 fp_xor_kernel(const uint8_t* __restrict__ data, size_t nbytes, size_t chunk_bytes, unsigned parts, int kind,
               unsigned long long* __restrict__ acc) {
+  pdl_begin();
   const size_t c = blockIdx.x / parts;
   const size_t b0 = c * chunk_bytes + size_t(blockIdx.x % parts) * kPartBytes;
   const size_t chunk_end = min(nbytes, (c + 1) * chunk_bytes);
@@ -181,19 +184,18 @@ cudaError_t launch_fingerprint(const void* data, size_t nbytes, int elem_size, i
   const unsigned np = unsigned(parts);
   if (mode == 0) {
     if ((reinterpret_cast<uintptr_t>(d) & 15) == 0)
-      fp_positional_kernel<true><<<grid, kThreads, 0, stream>>>(d, nbytes, chunk_bytes, np, acc);
+      e = launch_chained(fp_positional_kernel<true>, dim3(grid), dim3(kThreads), 0, stream, d, nbytes, chunk_bytes, np, acc);
     else
-      fp_positional_kernel<false><<<grid, kThreads, 0, stream>>>(d, nbytes, chunk_bytes, np, acc);
-    e = cudaGetLastError();
+      e = launch_chained(fp_positional_kernel<false>, dim3(grid), dim3(kThreads), 0, stream, d, nbytes, chunk_bytes, np, acc);
     if (e != cudaSuccess) return e;
-    fp_finalize_kernel<<<unsigned((nchunks + 255) / 256), 256, 0, stream>>>(acc, nchunks, nbytes, chunk_bytes);
-    return cudaGetLastError();
+    return launch_chained(fp_finalize_kernel, dim3(unsigned((nchunks + 255) / 256)), dim3(256), 0, stream, acc, nchunks,
+                          nbytes, chunk_bytes);
   }
   switch (elem_size) {
-    case 1: fp_xor_kernel<1><<<grid, kThreads, 0, stream>>>(d, nbytes, chunk_bytes, np, xor_kind, acc); break;
-    case 2: fp_xor_kernel<2><<<grid, kThreads, 0, stream>>>(d, nbytes, chunk_bytes, np, xor_kind, acc); break;
-    case 4: fp_xor_kernel<4><<<grid, kThreads, 0, stream>>>(d, nbytes, chunk_bytes, np, xor_kind, acc); break;
-    case 8: fp_xor_kernel<8><<<grid, kThreads, 0, stream>>>(d, nbytes, chunk_bytes, np, xor_kind, acc); break;
+    case 1: return launch_chained(fp_xor_kernel<1>, dim3(grid), dim3(kThreads), 0, stream, d, nbytes, chunk_bytes, np, xor_kind, acc);
+    case 2: return launch_chained(fp_xor_kernel<2>, dim3(grid), dim3(kThreads), 0, stream, d, nbytes, chunk_bytes, np, xor_kind, acc);
+    case 4: return launch_chained(fp_xor_kernel<4>, dim3(grid), dim3(kThreads), 0, stream, d, nbytes, chunk_bytes, np, xor_kind, acc);
+    case 8: return launch_chained(fp_xor_kernel<8>, dim3(grid), dim3(kThreads), 0, stream, d, nbytes, chunk_bytes, np, xor_kind, acc);
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

@@ -181,6 +181,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
     tc_fence_before();
   }
   // Expert offsets -> shared memory, validated, and the m-tile prefix.
+  pdl_begin();   // no global memory is touched above this line
   for (int e = tid; e <= E; e += NUM_THREADS) c.off[e] = p.offsets[e];
   __syncthreads();
   int bad = 0;
@@ -491,8 +492,7 @@ cudaError_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const KPar
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  grouped_gemm_kernel<MODE><<<grid, NUM_THREADS, kSmemBytes, stream>>>(ta, tb, kp);
-  return cudaGetLastError();
+  return launch_chained(grouped_gemm_kernel<MODE>, dim3(grid), dim3(NUM_THREADS), kSmemBytes, stream, ta, tb, kp);
 }
 
 }  // namespace

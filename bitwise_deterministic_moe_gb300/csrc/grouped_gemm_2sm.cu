@@ -204,6 +204,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
     tmem_relinquish_pair();
     tc_fence_before();
   }
+  pdl_begin();   // no global memory is touched above this line
   for (int e = tid; e <= E; e += NUM_THREADS) c.off[e] = p.offsets[e];
   __syncthreads();
   int bad = 0;
@@ -526,13 +527,15 @@ cudaError_t launch_pair_mode(const CUtensorMap& ta, const CUtensorMap& tb, const
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<MODE>, ta, tb, kp);
 }
 

@@ -26,6 +26,7 @@ constexpr int kEntriesPerBlock = 1024;
 __global__ void __launch_bounds__(32)
 hist_kernel(const int32_t* __restrict__ ids, long long R, int E, int nblk, int32_t* __restrict__ counts,
             int* status) {
+  pdl_begin();
   __shared__ int cnt[DMOE_MAX_EXPERTS];
   const int lane = threadIdx.x;
   const int b = blockIdx.x;
@@ -58,6 +59,7 @@ hist_kernel(const int32_t* __restrict__ ids, long long R, int E, int nblk, int32
 // One warp per expert: exclusive prefix over that expert's per-block counts.
 __global__ void __launch_bounds__(256)
 block_scan_kernel(int32_t* __restrict__ counts, int E, int nblk, int32_t* __restrict__ totals) {
+  pdl_begin();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= E) return;
@@ -81,6 +83,7 @@ block_scan_kernel(int32_t* __restrict__ counts, int E, int nblk, int32_t* __rest
 // Single CTA of 1024 threads: offsets[0..E] = exclusive scan of totals.
 __global__ void __launch_bounds__(1024)
 expert_scan_kernel(const int32_t* __restrict__ totals, int E, int32_t* __restrict__ offsets) {
+  pdl_begin();
   __shared__ int wsum[32];
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
@@ -112,6 +115,7 @@ expert_scan_kernel(const int32_t* __restrict__ totals, int E, int32_t* __restric
 __global__ void __launch_bounds__(32)
 scatter_kernel(const int32_t* __restrict__ ids, long long R, int E, int nblk, const int32_t* __restrict__ counts,
                const int32_t* __restrict__ offsets, int32_t* __restrict__ row_src) {
+  pdl_begin();
   __shared__ int next[DMOE_MAX_EXPERTS];
   const int lane = threadIdx.x;
   const int b = blockIdx.x;
@@ -156,11 +160,15 @@ cudaError_t launch_permute(const int32_t* topk_ids, long long R, int E, int32_t*
   const int nblk = int((R + kEntriesPerBlock - 1) / kEntriesPerBlock);
   int32_t* counts = static_cast<int32_t*>(scratch);
   int32_t* totals = counts + size_t(E) * nblk;
-  if (nblk > 0) hist_kernel<<<nblk, 32, 0, stream>>>(topk_ids, R, E, nblk, counts, status);
-  block_scan_kernel<<<(E * 32 + 255) / 256, 256, 0, stream>>>(counts, E, nblk, totals);
-  expert_scan_kernel<<<1, 1024, 0, stream>>>(totals, E, offsets);
-  if (nblk > 0) scatter_kernel<<<nblk, 32, 0, stream>>>(topk_ids, R, E, nblk, counts, offsets, row_src);
-  return cudaGetLastError();
+  cudaError_t e = cudaSuccess;
+  if (nblk > 0) e = launch_chained(hist_kernel, dim3(nblk), dim3(32), 0, stream, topk_ids, R, E, nblk, counts, status);
+  if (e == cudaSuccess)
+    e = launch_chained(block_scan_kernel, dim3((E * 32 + 255) / 256), dim3(256), 0, stream, counts, E, nblk, totals);
+  if (e == cudaSuccess) e = launch_chained(expert_scan_kernel, dim3(1), dim3(1024), 0, stream, totals, E, offsets);
+  if (e == cudaSuccess && nblk > 0)
+    e = launch_chained(scatter_kernel, dim3(nblk), dim3(32), 0, stream, topk_ids, R, E, nblk, counts, offsets,
+                       row_src);
+  return e;
 }
 
 }  // namespace dmoe
