@@ -205,3 +205,25 @@ def maxvio(topk_ids: np.ndarray, E: int) -> float:
     """Max expert load over mean load (the imbalance measure whose bound is E/topk)."""
     loads = expert_loads(topk_ids, E)
     return float(loads.max() / loads.mean())
+
+
+def hidden_states(cfg: MoEConfig) -> np.ndarray:
+    """Token hidden states in the latent dim, bf16 bits [T, N], N(0,1).
+
+    Input of the dispatch gather that forms the expert rows; drawn from its
+    own seeded blocks (tag 4), so it leaves every other input's bytes as they
+    are."""
+    return _normal_bf16(cfg.seed, 4, (cfg.T, cfg.N), 1.0)
+
+
+def dyadic_probs(T: int, topk: int) -> np.ndarray:
+    """Routing weights that are powers of two summing to exactly 1 per token
+    (1/2, 1/4, ..., with the last two equal), float32 [T, topk]."""
+    p = np.empty(topk, dtype=np.float64)
+    for j in range(topk):
+        p[j] = 2.0 ** -(j + 1)
+    if topk > 1:
+        p[-1] = p[-2]
+    else:
+        p[0] = 1.0
+    return np.broadcast_to(p.astype(np.float32), (T, topk)).copy()

@@ -20,6 +20,15 @@ Contents and the passage each part follows:
   About 2%", section "Interpretation".
 * ``combine`` -- dprob[t, j] from the per-row values: a scatter through
   row_src (the fixed-order slot combine reaches the plain dot product).
+* ``inverse_rows``, ``dispatch``, ``token_combine`` -- the steps either side
+  of the grouped GEMM: the gather that forms the expert-permuted rows from the
+  token hidden states, and the routing-probability-weighted combine of each
+  token's expert outputs.  Both are plain definitions (an index copy; a sum
+  over the token's choices in ascending j, binary64, then one rounding to
+  bf16).  The pages treat routing maps and dispatch outputs as order-sensitive
+  data to fingerprint ("NVIDIA fait passer ...", section "Méthodologie de
+  débogage du non-déterminisme"), and dprob is the derivative of this combine
+  with respect to the routing probability.
 * ``fingerprint`` -- chunk-wise tensor fingerprint with a header over dtype,
   shape and numel (same French page, section "Méthodologie de débogage du
   non-déterminisme": fingerprints computed on the GPU with shape, dtype and
@@ -213,6 +222,47 @@ def full(inputs, slot_width=SLOT_WIDTH):
                               slot_width=slot_width)
     dprob = combine(D, row_src, cfg.T, cfg.topk)
     return dict(off=off, row_src=row_src, Y=Y, Yb=Yb, P=P, D=D, dprob=dprob)
+
+
+# --------------------------------------------------------------------------
+# dispatch gather and token combine
+# --------------------------------------------------------------------------
+def inverse_rows(row_src) -> np.ndarray:
+    """row_of [R] int32 with row_src[row_of[f]] = f: the permuted row that holds
+    flat routing index f = t*topk + j.  row_src must be a permutation of [0,R)."""
+    row_src = np.asarray(row_src, dtype=np.int64).reshape(-1)
+    R = row_src.size
+    if R and not np.array_equal(np.sort(row_src), np.arange(R)):
+        raise ValueError("row_src is not a permutation")
+    row_of = np.empty(R, dtype=np.int32)
+    row_of[row_src] = np.arange(R, dtype=np.int32)
+    return row_of
+
+
+def dispatch(hidden, row_src, topk: int) -> np.ndarray:
+    """X_perm[r, :] = hidden[row_src[r] // topk, :]: the token's hidden state
+    copied (bf16 bits, unchanged) to every permuted row it was routed to."""
+    hidden = np.asarray(hidden, dtype=np.uint16)
+    tok = np.asarray(row_src, dtype=np.int64).reshape(-1) // topk
+    return hidden[tok]
+
+
+def token_combine(expert_out, probs, row_src, tokens=None):
+    """y[t, n] = sum over j = 0..topk-1 (ascending) of
+    prob[t, j] * expert_out[row_of[t*topk + j], n], in binary64 (each product of
+    a float32 and a bf16 is exact there), and its bf16 rounding.
+
+    Returns (y binary64 [ntok, N], y bf16 bits [ntok, N]) for the requested
+    tokens (all when None)."""
+    Yb = np.asarray(expert_out, dtype=np.uint16)
+    probs = np.asarray(probs, dtype=np.float32)
+    T, topk = probs.shape
+    row_of = inverse_rows(row_src).reshape(T, topk)
+    tokens = np.arange(T, dtype=np.int64) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    acc = np.zeros((tokens.size, Yb.shape[1]), dtype=np.float64)
+    for j in range(topk):
+        acc += probs[tokens, j].astype(np.float64)[:, None] * bf16_to_f64(Yb[row_of[tokens, j]])
+    return acc, bf16_rne(acc)
 
 
 # --------------------------------------------------------------------------
