@@ -218,6 +218,33 @@ def run_reference(args):
     return 0
 
 
+def dispatch_combine(api, cfg, inp, src, row_of, expert_out, timed, dev, iters):
+    """HBM roofline of the dispatch gather (hidden [T,N] -> x_perm [R,N]) and
+    the token combine (expert_out [R,N] -> y [T,N]) on the step's routing and
+    GEMM output.  Algorithmic bytes: gather = R*N*2 written + T*N*2 read once +
+    R*4 row ids; combine = R*N*2 read + T*N*2 written + R*4 row ids + R*4
+    weights.  x_perm and expert_out are larger than L2; hidden (T*N*2) is
+    meant to stay in L2 across its topk reads."""
+    import torch
+    pk, _ = peaks()
+    R, T, N = cfg.R, cfg.T, cfg.N
+    hidden = torch.from_numpy(synth.hidden_states(cfg).view(np.int16)).view(torch.bfloat16).to(dev)
+    probs = torch.from_numpy(inp.probs).to(dev)
+    xp = torch.empty(R, N, dtype=torch.bfloat16, device=dev)
+    y = torch.empty(T, N, dtype=torch.bfloat16, device=dev)
+    g_ms = timed(lambda: api.dispatch_gather(hidden, src, cfg.topk, out=xp), iters)
+    c_ms = timed(lambda: api.token_combine(expert_out, probs, row_of, out=y), iters)
+    res = {}
+    for name, ms, b in (("gather", g_ms, R * N * 2 + T * N * 2 + R * 4),
+                        ("combine", c_ms, R * N * 2 + T * N * 2 + R * 4 + R * 4)):
+        gbs = b / (ms * 1e-3) / 1e9
+        res[name] = {"ms": ms, "algorithmic_bytes": b, "achieved_gbs": gbs, "peak_gbs": pk["hbm_gbs"],
+                     "frac": gbs / pk["hbm_gbs"]}
+    del hidden, xp, y
+    torch.cuda.empty_cache()
+    return res
+
+
 # ---------------------------------------------------------------------------
 def run_ours(args):
     import torch
@@ -257,6 +284,7 @@ def run_ours(args):
     ws = api.workspace(T, k, cfg.E, dev)
     off = torch.empty(cfg.E + 1, dtype=torch.int32, device=dev)
     src = torch.empty(R, dtype=torch.int32, device=dev)
+    row_of = torch.empty(R, dtype=torch.int32, device=dev)
     out = torch.empty(R, cfg.N, dtype=torch.bfloat16, device=dev)
     slots = torch.empty(S, R, dtype=torch.float32, device=dev)
     dprob = torch.empty(T, k, dtype=torch.float32, device=dev)
@@ -266,7 +294,7 @@ def run_ours(args):
     launches_per_step = 4 + 2 + 2 + 2   # routing 4, fingerprint 2, GEMM + combine 2, fingerprint 2
 
     def step(ev=None):
-        api.permute_indices(ids, cfg.E, ws, off, src)
+        api.permute_indices(ids, cfg.E, ws, off, src, row_of=row_of)
         api.fingerprint(src, out=fp_src)
         if ev is not None:
             ev[0].record(stream)
@@ -355,6 +383,10 @@ def run_ours(args):
             torch.cuda.empty_cache()
     del dprob_a
 
+    # ---------------- the steps either side of the GEMM (not in the step)
+    around = None if args.skip_dispatch else dispatch_combine(api, cfg, inp, src, row_of, out, timed, dev,
+                                                              args.tax_iters)
+
     # ---------------- end to end through the public API, host buffers
     e2e = None
     if not args.skip_e2e:
@@ -424,6 +456,7 @@ def run_ours(args):
         "gpu_launches": launches_per_step * args.steps,
         "roofline": roof,
         "determinism_tax": tax,
+        "dispatch_combine": around,
         "e2e": e2e,
         "clocks": clocks,
     }
@@ -449,6 +482,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--skip-imbal", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--skip-dispatch", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

@@ -72,7 +72,9 @@ def load() -> ctypes.CDLL:
         "dmoe_version": ([], I),
         "dmoe_workspace_bytes": ([I, I, I], SZ),
         "dmoe_read_status": ([P, P], I),
-        "dmoe_permute_indices": ([P, I, I, I, P, P, P, SZ, P], I),
+        "dmoe_permute_indices": ([P, I, I, I, P, P, P, P, SZ, P], I),
+        "moe_dispatch_gather": ([P, P, I, I, I, P, P, SZ, P], I),
+        "moe_token_combine": ([P, P, P, I, I, I, P, P, SZ, P], I),
         "moe_grouped_gemm_fwd": ([P, P, P, I, I, I, I, P, LP, P, SZ, P], I),
         "moe_grouped_gemm_dprob": ([P, P, P, I, I, I, I, P, P, P, I, I, P, P, LP, P, SZ, P], I),
         "moe_grouped_gemm_dprob_atomic": ([P, P, P, I, I, I, I, P, P, P, I, I, P, LP, P, SZ, P], I),
@@ -137,7 +139,9 @@ def read_status(ws: torch.Tensor, stream=None) -> int:
 # ------------------------------------------------------------------ routing
 def permute_indices(topk_ids: torch.Tensor, E: int, ws: torch.Tensor,
                     expert_offsets: Optional[torch.Tensor] = None, row_src: Optional[torch.Tensor] = None,
-                    stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+                    stream=None, row_of: Optional[torch.Tensor] = None, with_row_of: bool = False):
+    """Returns (expert_offsets, row_src), plus row_of (the inverse map) when
+    with_row_of is set or a row_of buffer is passed."""
     _need(topk_ids, torch.int32, "topk_ids")
     T, topk = topk_ids.shape
     dev = topk_ids.device
@@ -147,10 +151,53 @@ def permute_indices(topk_ids: torch.Tensor, E: int, ws: torch.Tensor,
         row_src = torch.empty(T * topk, dtype=torch.int32, device=dev)
     _need(expert_offsets, torch.int32, "expert_offsets", (E + 1,))
     _need(row_src, torch.int32, "row_src", (T * topk,))
+    want = with_row_of or row_of is not None
+    if want and row_of is None:
+        row_of = torch.empty(T * topk, dtype=torch.int32, device=dev)
+    if row_of is not None:
+        _need(row_of, torch.int32, "row_of", (T * topk,))
     st = load().dmoe_permute_indices(_ptr(topk_ids), T, topk, E, _ptr(expert_offsets), _ptr(row_src),
-                                     _ptr(ws), ws.numel(), _stream(stream))
+                                     _ptr(row_of), _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "dmoe_permute_indices")
+    if want:
+        return expert_offsets, row_src, row_of
     return expert_offsets, row_src
+
+
+# ------------------------------------------------------------------ dispatch / combine
+def dispatch_gather(hidden, row_src, topk: int, ws=None, out=None, stream=None):
+    """x_perm [T*topk, H] = hidden[row_src // topk] (bits copied)."""
+    _need(hidden, hidden.dtype, "hidden")
+    if hidden.element_size() != 2 or hidden.dim() != 2:
+        raise TypeError("hidden must be a 2-D tensor of a 2-byte type")
+    T, H = hidden.shape
+    R = T * topk
+    if out is None:
+        out = torch.empty(R, H, dtype=hidden.dtype, device=hidden.device)
+    _need(out, hidden.dtype, "x_perm", (R, H))
+    _need(row_src, torch.int32, "row_src", (R,))
+    st = load().moe_dispatch_gather(_ptr(hidden), _ptr(row_src), T, topk, H, _ptr(out), _ptr(ws),
+                                    0 if ws is None else ws.numel(), _stream(stream))
+    _check(st, "moe_dispatch_gather")
+    return out
+
+
+def token_combine(expert_out, probs, row_of, ws=None, out=None, stream=None):
+    """y [T, N] bf16 = sum_j probs[t, j] * expert_out[row_of[t*topk + j]], fp32, j ascending."""
+    _need(expert_out, torch.bfloat16, "expert_out")
+    _need(probs, torch.float32, "probs")
+    T, topk = probs.shape
+    R, N = expert_out.shape
+    if R != T * topk:
+        raise ValueError("expert_out must have T*topk rows")
+    if out is None:
+        out = torch.empty(T, N, dtype=torch.bfloat16, device=expert_out.device)
+    _need(out, torch.bfloat16, "y", (T, N))
+    _need(row_of, torch.int32, "row_of", (R,))
+    st = load().moe_token_combine(_ptr(expert_out), _ptr(probs), _ptr(row_of), T, topk, N, _ptr(out), _ptr(ws),
+                                  0 if ws is None else ws.numel(), _stream(stream))
+    _check(st, "moe_token_combine")
+    return out
 
 
 # ------------------------------------------------------------------ GEMM

@@ -127,7 +127,8 @@ dmoe_status dmoe_read_status(void* ws, dmoe_stream_t stream) {
 }
 
 dmoe_status dmoe_permute_indices(const int32_t* topk_ids, int T, int topk, int E, int32_t* expert_offsets,
-                                 int32_t* row_src, void* ws, size_t ws_bytes, dmoe_stream_t stream) {
+                                 int32_t* row_src, int32_t* row_of, void* ws, size_t ws_bytes,
+                                 dmoe_stream_t stream) {
   if (T < 0 || topk < 0 || E < 1 || !expert_offsets) return DMOE_ERR_INVALID_ARG;
   if (E > DMOE_MAX_EXPERTS) return DMOE_ERR_UNSUPPORTED;
   const long long R = (long long)T * topk;
@@ -135,7 +136,7 @@ dmoe_status dmoe_permute_indices(const int32_t* topk_ids, int T, int topk, int E
   if (R > 0 && (!topk_ids || !row_src)) return DMOE_ERR_INVALID_ARG;
   if (!ws || ws_bytes < dmoe_workspace_bytes(T, topk, E)) return DMOE_ERR_WORKSPACE;
   void* scratch = static_cast<char*>(ws) + DMOE_WS_STATUS_BYTES;
-  return cuda_status(launch_permute(topk_ids, R, E, expert_offsets, row_src, scratch, status_ptr(ws),
+  return cuda_status(launch_permute(topk_ids, R, E, expert_offsets, row_src, row_of, scratch, status_ptr(ws),
                                     reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -236,6 +237,32 @@ dmoe_status moe_dprob_combine(const float* slots, const int32_t* row_src, int R,
   if (!slots || !row_src || !dprob || R < 0 || S < 1 || T < 0 || topk < 1) return DMOE_ERR_INVALID_ARG;
   if ((long long)T * topk != R) return DMOE_ERR_INVALID_ARG;
   return cuda_status(launch_dprob_combine(slots, row_src, R, S, dprob, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+dmoe_status moe_dispatch_gather(const void* hidden, const int32_t* row_src, int T, int topk, int H, void* x_perm,
+                                void* ws, size_t ws_bytes, dmoe_stream_t stream) {
+  if (T < 0 || topk < 1 || H < 1) return DMOE_ERR_INVALID_ARG;
+  const long long R = (long long)T * topk;
+  if (R >= (1ll << 31)) return DMOE_ERR_UNSUPPORTED;
+  if (H % 8 != 0 || H > 65536) return DMOE_ERR_UNSUPPORTED;
+  if (R > 0 && (!hidden || !row_src || !x_perm)) return DMOE_ERR_INVALID_ARG;
+  if (!aligned16(hidden) || !aligned16(x_perm)) return DMOE_ERR_INVALID_ARG;
+  if (ws && ws_bytes < DMOE_WS_STATUS_BYTES) return DMOE_ERR_WORKSPACE;
+  return cuda_status(launch_dispatch_gather(hidden, row_src, int(R), topk, H, x_perm, ws ? status_ptr(ws) : nullptr,
+                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
+dmoe_status moe_token_combine(const void* expert_out, const float* probs, const int32_t* row_of, int T, int topk,
+                              int N, void* y, void* ws, size_t ws_bytes, dmoe_stream_t stream) {
+  if (T < 0 || topk < 1 || N < 1) return DMOE_ERR_INVALID_ARG;
+  const long long R = (long long)T * topk;
+  if (R >= (1ll << 31)) return DMOE_ERR_UNSUPPORTED;
+  if (N % 8 != 0 || N > 65536 || topk > DMOE_COMBINE_MAX_TOPK) return DMOE_ERR_UNSUPPORTED;
+  if (T > 0 && (!expert_out || !probs || !row_of || !y)) return DMOE_ERR_INVALID_ARG;
+  if (!aligned16(expert_out) || !aligned16(y)) return DMOE_ERR_INVALID_ARG;
+  if (ws && ws_bytes < DMOE_WS_STATUS_BYTES) return DMOE_ERR_WORKSPACE;
+  return cuda_status(launch_token_combine(expert_out, probs, row_of, T, topk, N, int(R), y,
+                                          ws ? status_ptr(ws) : nullptr, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t dmoe_fingerprint_num_chunks(size_t nbytes, size_t chunk_bytes) {

@@ -34,7 +34,13 @@ cudaError_t launch_grouped_gemm_1sm(GemmMode mode, const GemmArgs& a, cudaStream
 // routing
 size_t routing_scratch_bytes(long long R, int E);
 cudaError_t launch_permute(const int32_t* topk_ids, long long R, int E, int32_t* offsets, int32_t* row_src,
-                           void* scratch, int* status, cudaStream_t stream);
+                           int32_t* row_of, void* scratch, int* status, cudaStream_t stream);
+
+// dispatch gather and token combine (status may be null: errors not recorded)
+cudaError_t launch_dispatch_gather(const void* hidden, const int32_t* row_src, int R, int topk, int H,
+                                   void* x_perm, int* status, cudaStream_t stream);
+cudaError_t launch_token_combine(const void* expert_out, const float* probs, const int32_t* row_of, int T,
+                                 int topk, int N, int R, void* y, int* status, cudaStream_t stream);
 
 // dprob (unfused epilogue and fixed-order combine)
 cudaError_t launch_dprob_epilogue(const void* grad_out, const void* expert_out, const int32_t* offsets,

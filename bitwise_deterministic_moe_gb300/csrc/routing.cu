@@ -14,6 +14,8 @@
 //   4. scatter: one warp per block walks its entries in order, 32 at a time;
 //      entries with equal ids are ranked by lane (match.any) and a per-expert
 //      running counter advances chunk by chunk, which keeps the sort stable.
+//      The same store can write the inverse map row_of[i] = position, which
+//      the token combine uses to find each (token, choice)'s row.
 // Scratch: counts int32 [E][nblk] and totals int32 [E].
 #include "common.cuh"
 #include "internal.h"
@@ -114,7 +116,8 @@ expert_scan_kernel(const int32_t* __restrict__ totals, int E, int32_t* __restric
 
 __global__ void __launch_bounds__(32)
 scatter_kernel(const int32_t* __restrict__ ids, long long R, int E, int nblk, const int32_t* __restrict__ counts,
-               const int32_t* __restrict__ offsets, int32_t* __restrict__ row_src) {
+               const int32_t* __restrict__ offsets, int32_t* __restrict__ row_src,
+               int32_t* __restrict__ row_of) {
   pdl_begin();
   __shared__ int next[DMOE_MAX_EXPERTS];
   const int lane = threadIdx.x;
@@ -141,6 +144,7 @@ scatter_kernel(const int32_t* __restrict__ ids, long long R, int E, int nblk, co
     __syncwarp();
     if (ok) {
       row_src[base + rank] = (int32_t)i;
+      if (row_of) row_of[i] = base + rank;
       if (rank == 0) next[e] = base + __popc(peers);
     }
     __syncwarp();
@@ -156,7 +160,7 @@ size_t routing_scratch_bytes(long long R, int E) {
 }
 
 cudaError_t launch_permute(const int32_t* topk_ids, long long R, int E, int32_t* offsets, int32_t* row_src,
-                           void* scratch, int* status, cudaStream_t stream) {
+                           int32_t* row_of, void* scratch, int* status, cudaStream_t stream) {
   const int nblk = int((R + kEntriesPerBlock - 1) / kEntriesPerBlock);
   int32_t* counts = static_cast<int32_t*>(scratch);
   int32_t* totals = counts + size_t(E) * nblk;
@@ -167,7 +171,7 @@ cudaError_t launch_permute(const int32_t* topk_ids, long long R, int E, int32_t*
   if (e == cudaSuccess) e = launch_chained(expert_scan_kernel, dim3(1), dim3(1024), 0, stream, totals, E, offsets);
   if (e == cudaSuccess && nblk > 0)
     e = launch_chained(scatter_kernel, dim3(nblk), dim3(32), 0, stream, topk_ids, R, E, nblk, counts, offsets,
-                       row_src);
+                       row_src, row_of);
   return e;
 }
 

@@ -116,13 +116,56 @@ dmoe_status dmoe_read_status(void* ws, dmoe_stream_t stream);
  *   topk_ids        int32 [T, topk], ids in [0, E) (duplicates allowed)
  *   expert_offsets  int32 [E+1] out: exclusive prefix of per-expert counts
  *   row_src         int32 [R]   out: flat index of each permuted row
+ *   row_of          int32 [R]   out, optional (may be null): the inverse,
+ *                   row_of[t*topk + j] = the row that holds (t, j), as used by
+ *                   moe_token_combine
  * Positions come from per-block counts and prefix sums, never from atomic
  * position tickets.  An id outside [0,E) sets DMOE_ERR_ROUTING in ws; the
  * outputs are then undefined.  T*topk may be 0.
  */
 dmoe_status dmoe_permute_indices(const int32_t* topk_ids, int T, int topk, int E,
-                                 int32_t* expert_offsets, int32_t* row_src,
+                                 int32_t* expert_offsets, int32_t* row_src, int32_t* row_of,
                                  void* ws, size_t ws_bytes, dmoe_stream_t stream);
+
+/*
+ * Dispatch gather: the expert-permuted input rows from the token hidden
+ * states, the step before the experts.  Every (token, choice) row is a copy:
+ *     x_perm[r, :] = hidden[row_src[r] / topk, :]        (bits unchanged)
+ * Dispatch outputs are order-sensitive data ("NVIDIA fait passer ...",
+ * section "Méthodologie de débogage du non-déterminisme"); the row order is
+ * the fixed one of dmoe_permute_indices, so x_perm is identical run to run.
+ *   hidden   bf16 [T, H]      (any 2-byte type: only bits are moved)
+ *   row_src  int32 [T*topk]   from dmoe_permute_indices
+ *   x_perm   bf16 [T*topk, H] out
+ * H % 8 == 0, H <= 65536 (16-byte rows); hidden and x_perm 16-byte aligned.
+ * ws: null, or a workspace of at least DMOE_WS_STATUS_BYTES whose status word
+ * receives DMOE_ERR_ROUTING for a row_src entry outside [0, T*topk) (that
+ * row is then left unwritten).  T may be 0.
+ */
+dmoe_status moe_dispatch_gather(const void* hidden, const int32_t* row_src, int T, int topk, int H,
+                                void* x_perm, void* ws, size_t ws_bytes, dmoe_stream_t stream);
+
+/*
+ * Token combine: each token's output is the routing-probability-weighted sum
+ * of its expert output rows, the step after the experts and the function
+ * whose derivative with respect to prob is dprob ("Trillion-Parameter
+ * Pretraining ...", section "Interpretation"):
+ *     y[t, n] = bf16_rn( sum_{j = 0..topk-1} prob[t, j] * expert_out[row_of[t*topk + j], n] )
+ * accumulated in fp32 as a fused multiply-add chain from +0 in ascending j,
+ * then rounded once to bf16 (nearest even).  One thread owns each output
+ * vector, so the bits never depend on the grid or on scheduling.
+ *   expert_out  bf16 [T*topk, N]   permuted rows (moe_grouped_gemm_* output)
+ *   probs       fp32 [T, topk]
+ *   row_of      int32 [T*topk]     from dmoe_permute_indices
+ *   y           bf16 [T, N]        out
+ * N % 8 == 0, N <= 65536, topk <= DMOE_COMBINE_MAX_TOPK; expert_out and y
+ * 16-byte aligned.  ws as for moe_dispatch_gather: a row_of entry outside
+ * [0, T*topk) records DMOE_ERR_ROUTING and that term is dropped.
+ */
+#define DMOE_COMBINE_MAX_TOPK 64
+dmoe_status moe_token_combine(const void* expert_out, const float* probs, const int32_t* row_of,
+                              int T, int topk, int N, void* y, void* ws, size_t ws_bytes,
+                              dmoe_stream_t stream);
 
 /*
  * Grouped GEMM (FFN-out projection into the latent dim): for every expert e

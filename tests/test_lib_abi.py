@@ -30,7 +30,7 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for want in ["moe_grouped_gemm_fwd", "moe_grouped_gemm_dprob", "moe_grouped_gemm_dprob_atomic",
                  "moe_dprob_epilogue", "moe_dprob_combine", "dmoe_permute_indices", "dmoe_fingerprint",
-                 "dmoe_read_status", "dmoe_workspace_bytes"]:
+                 "dmoe_read_status", "dmoe_workspace_bytes", "moe_dispatch_gather", "moe_token_combine"]:
         assert want in names
 
 
@@ -75,11 +75,27 @@ def test_invalid_arguments_rejected_on_host(lib):
     # R != T * topk -> invalid argument
     assert g(16, 16, 16, 10, 2, 64, 256, 16, 16, 16, 3, 4, 16, 16, None, 16, 4096, None) == 1
     p = lib.dmoe_permute_indices
-    p.argtypes = [P, I, I, I, P, P, P, SZ, P]
+    p.argtypes = [P, I, I, I, P, P, P, P, SZ, P]
     p.restype = I
-    assert p(16, 4, 2, 0, 16, 16, 16, 4096, None) == 1          # E = 0
-    assert p(16, 4, 2, 4096, 16, 16, 16, 4096, None) == 2       # E > 1024
-    assert p(16, 4, 2, 8, 16, 16, 16, 8, None) == 6             # workspace too small
+    assert p(16, 4, 2, 0, 16, 16, None, 16, 4096, None) == 1          # E = 0
+    assert p(16, 4, 2, 4096, 16, 16, None, 16, 4096, None) == 2       # E > 1024
+    assert p(16, 4, 2, 8, 16, 16, 16, 16, 8, None) == 6               # workspace too small
+    d = lib.moe_dispatch_gather
+    d.argtypes = [P, P, I, I, I, P, P, SZ, P]
+    d.restype = I
+    assert d(16, 16, 4, 2, 12, 16, None, 0, None) == 2       # H not a multiple of 8
+    assert d(8, 16, 4, 2, 16, 16, None, 0, None) == 1        # misaligned hidden
+    assert d(None, 16, 4, 2, 16, 16, None, 0, None) == 1     # null hidden
+    assert d(16, 16, 4, 2, 16, 16, 16, 8, None) == 6         # workspace below the status region
+    assert d(None, None, 0, 2, 16, None, None, 0, None) == 0  # no tokens: nothing to launch
+    c = lib.moe_token_combine
+    c.argtypes = [P, P, P, I, I, I, P, P, SZ, P]
+    c.restype = I
+    assert c(16, 16, 16, 4, 65, 16, 16, None, 0, None) == 2   # topk above the combine's limit
+    assert c(16, 16, 16, 4, 2, 20, 16, None, 0, None) == 2    # N not a multiple of 8
+    assert c(16, 16, 16, 4, 0, 16, 16, None, 0, None) == 1    # topk = 0
+    assert c(16, 16, 16, 4, 2, 16, 24, None, 0, None) == 1    # misaligned y
+    assert c(None, None, None, 0, 2, 16, None, None, 0, None) == 0
     fp = lib.dmoe_fingerprint
     fp.argtypes = [P, SZ, I, I, ctypes.POINTER(ctypes.c_int64), SZ, I, P, ctypes.POINTER(ctypes.c_uint64), P]
     fp.restype = I
