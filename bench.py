@@ -10,7 +10,9 @@ top-22, K=1024, N=2048 latent, Zipf(1.1) expert popularity):
   4. chunk fingerprint of dprob
 The metric is algorithmic grouped-GEMM TFLOP/s (2*R*K*N per step) over the
 whole step time.  The determinism tax compares the deterministic GEMM call
-with the atomicAdd control (memset + moe_grouped_gemm_dprob_atomic).
+with the atomicAdd control (memset + moe_grouped_gemm_dprob_atomic); the
+serialized-writer control (moe_grouped_gemm_dprob_serial: deterministic, the
+N-tiles of a row block take turns) is timed beside them.
 
 Usage: python bench.py [--gpus N --steps K --warmup W] [--impl reference]
 For N > 1 (torchrun) every rank runs an independent replica on its own GPU
@@ -368,16 +370,21 @@ def run_ours(args):
         tsl = torch.empty(tcfg.S, tcfg.R, dtype=torch.float32, device=dev)
         tdp = torch.empty(tcfg.T, tcfg.topk, dtype=torch.float32, device=dev)
         tda = torch.empty_like(tdp)
-        det_ms, atom_ms = [], []
+        det_ms, atom_ms, ser_ms = [], [], []
         for _ in range(3):   # interleave to share clock/thermal conditions
             det_ms.append(timed(lambda: api.grouped_gemm_dprob(tX, tW, toff, tG, tsrc, tcfg.topk, tws, out=to,
                                                                slots=tsl, dprob=tdp), args.tax_iters))
             atom_ms.append(timed(lambda: api.grouped_gemm_dprob_atomic(tX, tW, toff, tG, tsrc, tcfg.topk, tws,
                                                                        out=to, dprob=tda), args.tax_iters))
-        d, a = float(np.median(det_ms)), float(np.median(atom_ms))
+            ser_ms.append(timed(lambda: api.grouped_gemm_dprob_serial(tX, tW, toff, tG, tsrc, tcfg.topk, tws,
+                                                                      out=to, dprob=tda), args.tax_iters))
+        if api.read_status(tws) != 0:
+            raise RuntimeError("device status set while timing the controls")
+        d, a, sr = float(np.median(det_ms)), float(np.median(atom_ms)), float(np.median(ser_ms))
         tf, _ = algorithmic(tcfg, toff.cpu().numpy())
         tax[name] = {"det_ms": d, "atomic_ms": a, "tax_pct": (d / a - 1.0) * 100.0,
-                     "det_tflops": tf / (d * 1e-3) / 1e12}
+                     "det_tflops": tf / (d * 1e-3) / 1e12,
+                     "serial_ms": sr, "serial_tax_pct": (sr / a - 1.0) * 100.0}
         if name != args.config:
             del tX, tW, tG, to, tsl, tdp, tda
             torch.cuda.empty_cache()

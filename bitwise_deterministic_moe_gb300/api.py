@@ -78,6 +78,7 @@ def load() -> ctypes.CDLL:
         "moe_grouped_gemm_fwd": ([P, P, P, I, I, I, I, P, LP, P, SZ, P], I),
         "moe_grouped_gemm_dprob": ([P, P, P, I, I, I, I, P, P, P, I, I, P, P, LP, P, SZ, P], I),
         "moe_grouped_gemm_dprob_atomic": ([P, P, P, I, I, I, I, P, P, P, I, I, P, LP, P, SZ, P], I),
+        "moe_grouped_gemm_dprob_serial": ([P, P, P, I, I, I, I, P, P, P, I, I, P, LP, P, SZ, P], I),
         "moe_dprob_epilogue": ([P, P, P, P, I, I, I, I, I, P, P], I),
         "moe_dprob_combine": ([P, P, I, I, I, I, P, P], I),
         "dmoe_fingerprint_num_chunks": ([SZ, SZ], SZ),
@@ -268,6 +269,27 @@ def grouped_gemm_dprob_atomic(X_perm, W, expert_offsets, grad_out, row_src, topk
                                               _ptr(grad_out), _ptr(row_src), T, topk, _ptr(dprob),
                                               _launch(num_ctas, flags), _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "moe_grouped_gemm_dprob_atomic")
+    return out, dprob
+
+
+def grouped_gemm_dprob_serial(X_perm, W, expert_offsets, grad_out, row_src, topk: int, ws, out=None, dprob=None,
+                              num_ctas: int = 0, stream=None, flags: int = 0):
+    """Serialized-writer control (deterministic, no slots): returns (expert_out, dprob)."""
+    R, E, K, N = _gemm_shapes(X_perm, W, expert_offsets)
+    T = R // topk
+    dev = X_perm.device
+    if out is None:
+        out = torch.empty(R, N, dtype=torch.bfloat16, device=dev)
+    if dprob is None:
+        dprob = torch.empty(T, topk, dtype=torch.float32, device=dev)
+    _need(out, torch.bfloat16, "expert_out", (R, N))
+    _need(grad_out, torch.bfloat16, "grad_out", (T, N))
+    _need(row_src, torch.int32, "row_src", (R,))
+    _need(dprob, torch.float32, "dprob", (T, topk))
+    st = load().moe_grouped_gemm_dprob_serial(_ptr(X_perm), _ptr(W), _ptr(expert_offsets), R, E, K, N, _ptr(out),
+                                              _ptr(grad_out), _ptr(row_src), T, topk, _ptr(dprob),
+                                              _launch(num_ctas, flags), _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "moe_grouped_gemm_dprob_serial")
     return out, dprob
 
 

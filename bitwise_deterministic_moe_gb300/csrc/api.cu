@@ -108,7 +108,13 @@ int dmoe_version(void) { return 10000; }
 
 size_t dmoe_workspace_bytes(int T, int topk, int E) {
   if (T < 0 || topk < 0 || E < 1) return 0;
-  return DMOE_WS_STATUS_BYTES + routing_scratch_bytes((long long)T * topk, E);
+  // the region after the status word is the routing scratch, reused as the
+  // serialized control's counters (calls sharing a workspace are ordered)
+  const long long R = (long long)T * topk;
+  size_t scratch = routing_scratch_bytes(R, E);
+  const size_t flags = (serial_flag_bytes(R, E) + 255) & ~size_t(255);
+  if (flags > scratch) scratch = flags;
+  return DMOE_WS_STATUS_BYTES + scratch;
 }
 
 dmoe_status dmoe_read_status(void* ws, dmoe_stream_t stream) {
@@ -217,6 +223,39 @@ dmoe_status moe_grouped_gemm_dprob_atomic(const void* X_perm, const void* W, con
   a.flags = launch ? launch->flags : 0;
   if (a.num_ctas < 0) return DMOE_ERR_INVALID_ARG;
   return cuda_status(launch_grouped_gemm(GemmMode::kAtomic, a, s));
+}
+
+dmoe_status moe_grouped_gemm_dprob_serial(const void* X_perm, const void* W, const int32_t* expert_offsets, int R,
+                                          int E, int K, int N, void* expert_out, const void* grad_out,
+                                          const int32_t* row_src, int T, int topk, float* dprob,
+                                          const dmoe_launch* launch, void* ws, size_t ws_bytes,
+                                          dmoe_stream_t stream) {
+  dmoe_status st = check_gemm_shape(X_perm, W, expert_offsets, R, E, K, N, expert_out, ws, ws_bytes);
+  if (st != DMOE_OK) return st;
+  st = check_dprob_args(grad_out, row_src, R, T, topk);
+  if (st != DMOE_OK) return st;
+  if (!dprob) return DMOE_ERR_INVALID_ARG;
+  const size_t fbytes = serial_flag_bytes(R, E);
+  if (ws_bytes < DMOE_WS_STATUS_BYTES + fbytes) return DMOE_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int* wflags = reinterpret_cast<int*>(static_cast<char*>(ws) + DMOE_WS_STATUS_BYTES);
+  if (R > 0) {
+    cudaError_t e = cudaMemsetAsync(wflags, 0, fbytes, s);
+    if (e != cudaSuccess) return DMOE_ERR_CUDA;
+  }
+  GemmArgs a{};
+  a.X = X_perm; a.W = W; a.offsets = expert_offsets;
+  a.R = R; a.E = E; a.K = K; a.N = N;
+  a.out = expert_out;
+  a.grad_out = grad_out; a.row_src = row_src; a.topk = topk;
+  a.dprob = dprob;
+  a.wflags = wflags;
+  a.status = status_ptr(ws);
+  a.sched = sched_ptr(ws);
+  a.num_ctas = launch ? launch->num_ctas : 0;
+  a.flags = launch ? launch->flags : 0;
+  if (a.num_ctas < 0) return DMOE_ERR_INVALID_ARG;
+  return cuda_status(launch_grouped_gemm(GemmMode::kSerial, a, s));
 }
 
 dmoe_status moe_dprob_epilogue(const void* grad_out, const void* expert_out, const int32_t* expert_offsets,

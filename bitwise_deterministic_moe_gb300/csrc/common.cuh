@@ -160,6 +160,36 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, u
   return true;
 }
 
+// Global-memory counter written by another CTA: acquire-load and publish.
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(int* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Bounded wait (one thread) until *ctr >= target.  Same failure rules as
+// mbar_wait_t: gives up when *abort is raised elsewhere, or after limit_ns,
+// recording DMOE_ERR_TIMEOUT and raising *abort.
+__device__ __forceinline__ bool counter_wait(const int* ctr, int target, volatile int* abort, int* status,
+                                             unsigned long long limit_ns) {
+  if (ld_acquire_gpu(ctr) >= target) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (;;) {
+    __nanosleep(128);
+    if (ld_acquire_gpu(ctr) >= target) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      record_error(status, DMOE_ERR_TIMEOUT);
+      *abort = 1;
+      return false;
+    }
+  }
+}
+
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }

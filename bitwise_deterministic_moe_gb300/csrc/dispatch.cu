@@ -41,10 +41,8 @@ dispatch_gather_kernel(const uint4* __restrict__ hidden, const int32_t* __restri
   const uint64_t keep = policy_evict_last();
   const uint64_t stream = policy_evict_first();
   const long long nsrc = (long long)R;   // flat routing indices live in [0, R)
-  int src_next = (warp < R) ? __ldg(row_src + warp) : 0;
   for (int r = warp; r < R; r += nwarps) {
-    const int src = src_next;
-    if ((long long)r + nwarps < R) src_next = __ldg(row_src + r + nwarps);   // next row's id, in flight early
+    const int src = __ldg(row_src + r);
     if (src < 0 || src >= nsrc) {
       if (lane == 0) record_error(status, DMOE_ERR_ROUTING);
       continue;

@@ -81,6 +81,7 @@ struct KParams {
   int topk;
   float* slots;
   float* dprob;
+  int* wflags;  // serialized writers: slots already added per (m-tile, row quarter); zero at launch
   int* status;
   int* sched;   // [0] next-tile counter, [1] finished-CTA counter; zero between launches
   unsigned long long wait_ns;   // limit of every pipeline wait
@@ -237,15 +238,23 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
       // global counter), so neighbouring tiles -- which share weight slices
       // and X rows in L2 -- run at nearly the same time on different SMs.
       // Which CTA computes a tile never changes its bits.
-      int tile = blockIdx.x;
+      // The serialized control claims every tile from the counter, so a tile
+      // is owned only by a CTA that is already running: its writers wait on
+      // earlier-claimed tiles only, which always make progress.
+      constexpr bool kClaimAll = MODE == int(GemmMode::kSerial);
+      int tile = kClaimAll ? atomicAdd(p.sched, 1) : int(blockIdx.x);
       for (int qi = 0;; ++qi) {
         const int qs = qi % TQ;
         if (!mbar_wait(smem_u32(&c.tq_empty[qs]), uint32_t((qi / TQ) & 1) ^ 1u, &c.abort, p.status, p.wait_ns)) break;
-        const int cur = tile < total_tiles ? tile : -1;
+        // the serialized control claims n-tile-major (every m-tile's n-tile 0,
+        // then every n-tile 1, ...), so a writer's predecessor was claimed a
+        // whole round earlier; queued tiles carry the usual unit-major index
+        const int cur = tile >= total_tiles ? -1
+                        : kClaimAll ? (tile % units) * p.NT + tile / units : tile;
         c.tq_tile[qs] = cur;
         mbar_arrive(smem_u32(&c.tq_full[qs]));
         if (cur < 0) break;
-        tile = int(gridDim.x) + atomicAdd(p.sched, 1);   // fetched early: latency hides behind the loads
+        tile = (kClaimAll ? 0 : int(gridDim.x)) + atomicAdd(p.sched, 1);   // fetched early: latency hides behind the loads
         const Tile tl = decode_tile(cur, c, E, p.NT, units_heavy, units);
         const int brow = tl.e * p.N + tl.n0;
         bool ok = true;
@@ -407,18 +416,44 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
           __syncwarp();
         }
         if (MODE != int(GemmMode::kFwd)) {
+          float parts[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             // part k4 of row rr[i]; combine the four parts as (L0 + L1) + (L2 + L3)
             float part = slot_tree(a[i]);
             part = __fadd_rn(part, __shfl_xor_sync(0xffffffffu, part, 1));
             part = __fadd_rn(part, __shfl_xor_sync(0xffffffffu, part, 2));
+            parts[i] = part;
             if (k4 == 0 && ok[i]) {
               if (MODE == int(GemmMode::kSlots))
                 p.slots[size_t(col0 / SLOT) * p.R + rr[i]] = part;
-              else
+              else if (MODE == int(GemmMode::kAtomic))
                 atomicAdd(p.dprob + src[i], part);
             }
+          }
+          if (MODE == int(GemmMode::kSerial)) {
+            // Serialized writers: slot s of these 32 rows is added into dprob
+            // only after slots 0..s-1 have been, so dprob = ((P0 + P1) + P2) + ...
+            // -- the fixed-order combine's bits -- but the tiles of one
+            // m-tile wait on one another instead of writing in parallel.
+            const int s = col0 / SLOT;
+            int* ctr = p.wflags + size_t(cur / p.NT) * 4 + q;
+            int go = 1;
+            if (lane == 0) go = counter_wait(ctr, s, &c.abort, p.status, p.wait_ns) ? 1 : 0;
+            go = __shfl_sync(0xffffffffu, go, 0);
+            __syncwarp();
+            if (!go) break;
+            __threadfence();
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              if (k4 == 0 && ok[i]) {
+                float* d = p.dprob + src[i];
+                __stcg(d, s == 0 ? parts[i] : __fadd_rn(__ldcg(d), parts[i]));
+              }
+            }
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) st_release_gpu(ctr, s + 1);
           }
         }
       }
@@ -497,6 +532,11 @@ cudaError_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const KPar
 
 }  // namespace
 
+size_t serial_flag_bytes(long long R, int E) {
+  // m-tiles <= R/BM + E (at most one partial tile per expert), four row quarters each
+  return size_t(R / BM + E + 1) * 4 * sizeof(int);
+}
+
 cudaError_t launch_grouped_gemm_1sm(GemmMode mode, const GemmArgs& a, cudaStream_t stream) {
   if (a.R == 0) return cudaSuccess;
   CUtensorMap ta, tb;
@@ -516,16 +556,19 @@ cudaError_t launch_grouped_gemm_1sm(GemmMode mode, const GemmArgs& a, cudaStream
   kp.topk = a.topk;
   kp.slots = a.slots;
   kp.dprob = a.dprob;
+  kp.wflags = a.wflags;
   kp.status = a.status;
   kp.sched = a.sched;
   if (!kp.sched) return cudaErrorInvalidValue;
   kp.stall_test = (a.flags & DMOE_LAUNCH_TEST_STALL) ? 1 : 0;
   kp.wait_ns = kp.stall_test ? 200ull * 1000ull * 1000ull : kWaitLimitNs;   // a short limit for the test
   int grid = a.num_ctas > 0 ? a.num_ctas : device_sm_count();
+  if (mode == GemmMode::kSerial && !kp.wflags) return cudaErrorInvalidValue;
   switch (mode) {
     case GemmMode::kFwd: return launch_mode<int(GemmMode::kFwd)>(ta, tb, kp, grid, stream);
     case GemmMode::kSlots: return launch_mode<int(GemmMode::kSlots)>(ta, tb, kp, grid, stream);
     case GemmMode::kAtomic: return launch_mode<int(GemmMode::kAtomic)>(ta, tb, kp, grid, stream);
+    case GemmMode::kSerial: return launch_mode<int(GemmMode::kSerial)>(ta, tb, kp, grid, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -610,7 +610,8 @@ constexpr long long kPairMinMeanRows = 512;
 
 cudaError_t launch_grouped_gemm(GemmMode mode, const GemmArgs& a, cudaStream_t stream) {
   bool pairs;
-  if (a.flags & DMOE_LAUNCH_SINGLE_CTA) pairs = false;
+  if (mode == GemmMode::kSerial) pairs = false;   // the serialized control has one kernel
+  else if (a.flags & DMOE_LAUNCH_SINGLE_CTA) pairs = false;
   else if (a.flags & DMOE_LAUNCH_CTA_PAIRS) pairs = true;
   else pairs = (long long)a.R >= kPairMinMeanRows * a.E;
   if (!pairs) return launch_grouped_gemm_1sm(mode, a, stream);

@@ -9,7 +9,7 @@
 
 namespace dmoe {
 
-enum class GemmMode : int { kFwd = 0, kSlots = 1, kAtomic = 2 };
+enum class GemmMode : int { kFwd = 0, kSlots = 1, kAtomic = 2, kSerial = 3 };
 
 struct GemmArgs {
   const void* X;              // bf16 [R, K]
@@ -21,7 +21,9 @@ struct GemmArgs {
   const int32_t* row_src;     // [R]           (slots / atomic)
   int topk;
   float* slots;               // [S, R]        (slots)
-  float* dprob;               // [T*topk]      (atomic)
+  float* dprob;               // [T*topk]      (atomic, serial)
+  int* wflags;                // serial: per (m-tile, row quarter) count of slots already added; zeroed
+                              // by the launcher before each launch
   int* status;                // device status word (may be null: errors not recorded)
   int* sched;                 // 2 device ints, zero between launches: dynamic tile counter
   int num_ctas;               // 0 = one per SM
@@ -30,6 +32,9 @@ struct GemmArgs {
 
 cudaError_t launch_grouped_gemm(GemmMode mode, const GemmArgs& a, cudaStream_t stream);       // CTA pairs
 cudaError_t launch_grouped_gemm_1sm(GemmMode mode, const GemmArgs& a, cudaStream_t stream);   // single CTAs
+
+// serialized-writer control: bytes of its per-(m-tile, row quarter) counters
+size_t serial_flag_bytes(long long R, int E);
 
 // routing
 size_t routing_scratch_bytes(long long R, int E);

@@ -98,7 +98,8 @@ int dmoe_version(void);
 
 /* Workspace needed by every call below for a problem with T tokens, topk
  * choices and E experts (status word, the grouped GEMM's tile counters, and
- * routing scratch).  The caller allocates it once, ZERO-FILLED, and may reuse
+ * routing scratch, which the serialized-writer control reuses for its turn
+ * counters).  The caller allocates it once, ZERO-FILLED, and may reuse
  * it for every call on that problem size; every call leaves the counters at
  * zero.  Calls that share a workspace must be ordered on one stream. */
 size_t dmoe_workspace_bytes(int T, int topk, int E);
@@ -220,6 +221,37 @@ dmoe_status moe_grouped_gemm_dprob(const void* X_perm, const void* W, const int3
  * determinism tax.
  */
 dmoe_status moe_grouped_gemm_dprob_atomic(const void* X_perm, const void* W, const int32_t* expert_offsets,
+                                          int R, int E, int K, int N, void* expert_out,
+                                          const void* grad_out, const int32_t* row_src, int T, int topk,
+                                          float* dprob,
+                                          const dmoe_launch* launch, void* ws, size_t ws_bytes,
+                                          dmoe_stream_t stream);
+
+/*
+ * The serialized-writer control: deterministic without private slots.  The
+ * same GEMM and per-slot partials, but the writers of one row take turns:
+ * slot s of a block of 32 rows is added into dprob only after slots
+ * 0..s-1 of those rows have been (a counter per m-tile and row quarter in
+ * the workspace, acquire/release ordered), so
+ *     dprob[row_src[r]] = ((P[0,r] + P[1,r]) + P[2,r]) + ...
+ * bitwise equal to moe_grouped_gemm_dprob, while the N-tiles of one m-tile
+ * wait on one another instead of writing in parallel -- the parallelism the
+ * pages say serialising gives up ("Trillion-Parameter Pretraining ...",
+ * section "Interpretation").  Kept only as a timing point between the
+ * atomic control and the private-slot path.
+ *  - Always runs the single-CTA kernel (DMOE_LAUNCH_CTA_PAIRS is ignored).
+ *  - Every tile is claimed from the workspace counter by a CTA already
+ *    running, in n-tile-major order (n-tile 0 of every m-tile, then n-tile
+ *    1, ...), so a writer only waits on earlier-claimed tiles held by running
+ *    CTAs and the turns always advance, whatever num_ctas is.  (In the
+ *    m-tile-major order of the other calls the turns convoy behind the tile
+ *    queues; n-tile-major gives up the X-row reuse in L2 instead.)
+ *  - Uses the workspace region after the status word (dmoe_workspace_bytes
+ *    covers it) and zero-fills it on `stream` before the kernel.
+ *  - A turn that does not come within the wait limit records
+ *    DMOE_ERR_TIMEOUT; outputs are then undefined.
+ */
+dmoe_status moe_grouped_gemm_dprob_serial(const void* X_perm, const void* W, const int32_t* expert_offsets,
                                           int R, int E, int K, int N, void* expert_out,
                                           const void* grad_out, const int32_t* row_src, int T, int topk,
                                           float* dprob,

@@ -53,3 +53,19 @@ def test_corrupt_row_src_is_reported_not_followed():
     api.dprob_combine(slots, src, prob.cfg.topk, dprob=dp)
     torch.cuda.synchronize()
     assert api.read_status(prob.ws) == 0
+
+
+def test_serialized_writers_timeout_then_recover():
+    """A stalled stage in the serialized control: the stalled CTA and every
+    writer waiting for its turn give up within their limits, the status says
+    DMOE_ERR_TIMEOUT, and the next call gives the deterministic bits."""
+    prob = Problem(synth.CONFIGS["small"])
+    _, ref_dp, _ = prob.run_dprob()
+    ref_dp = bits(ref_dp)
+    assert api.read_status(prob.ws) == 0
+    api.grouped_gemm_dprob_serial(prob.X, prob.W, prob.off, prob.G, prob.src, prob.cfg.topk, prob.ws,
+                                  flags=api.LAUNCH_TEST_STALL)
+    assert api.read_status(prob.ws) == 4
+    _, dp = api.grouped_gemm_dprob_serial(prob.X, prob.W, prob.off, prob.G, prob.src, prob.cfg.topk, prob.ws)
+    assert api.read_status(prob.ws) == 0
+    assert torch.equal(bits(dp), ref_dp)

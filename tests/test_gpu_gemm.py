@@ -152,3 +152,32 @@ def test_single_and_pair_kernels_bitwise_equal(name):
     assert torch.equal(s1.view(torch.int32), s2.view(torch.int32))
     assert torch.equal(d1.view(torch.int32), d2.view(torch.int32))
     assert api.read_status(prob.ws) == 0
+
+
+@pytest.mark.parametrize("num_ctas", [0, 37, 1])
+@pytest.mark.parametrize("cfg", SHAPES, ids=[c.name for c in SHAPES])
+def test_serialized_writers_bitwise_equal_to_slots(cfg, num_ctas):
+    """The serialized-writer control adds the slots into dprob in ascending
+    order as they come, so it must give the fixed-order combine's bits (and the
+    same expert_out) for any grid, including a single CTA that holds every
+    turn itself."""
+    prob = Problem(cfg)
+    out, dprob, _ = prob.run_dprob(flags=api.LAUNCH_SINGLE_CTA)
+    out, dprob = out.clone(), dprob.clone()
+    out_s, dprob_s = api.grouped_gemm_dprob_serial(prob.X, prob.W, prob.off, prob.G, prob.src, cfg.topk, prob.ws,
+                                                   num_ctas=num_ctas)
+    assert api.read_status(prob.ws) == 0
+    assert torch.equal(out.view(torch.int16), out_s.view(torch.int16))
+    assert torch.equal(dprob.view(torch.int32), dprob_s.view(torch.int32))
+
+
+@pytest.mark.parametrize("name", ["latent", "imbal"])
+def test_serialized_writers_full_size(name):
+    prob = Problem(synth.CONFIGS[name])
+    _, dprob, _ = prob.run_dprob()
+    dprob = dprob.clone()
+    for _ in range(2):
+        _, dprob_s = api.grouped_gemm_dprob_serial(prob.X, prob.W, prob.off, prob.G, prob.src, prob.cfg.topk,
+                                                   prob.ws)
+        assert api.read_status(prob.ws) == 0
+        assert torch.equal(dprob.view(torch.int32), dprob_s.view(torch.int32))
