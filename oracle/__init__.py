@@ -29,6 +29,12 @@ Contents and the passage each part follows:
   data to fingerprint ("NVIDIA fait passer ...", section "Méthodologie de
   débogage du non-déterminisme"), and dprob is the derivative of this combine
   with respect to the routing probability.
+* ``wgrad_entries`` / ``wgrad_expert`` -- the grouped GEMM's weight gradient
+  dW[e] = dY_e^T X_e over the expert's rows (binary64, rows ascending).  A
+  weight-gradient path is one of the three workloads whose determinism
+  overhead the pages measure ("Trillion-Parameter Pretraining ...", section
+  "Synopsis"; "NVIDIA fait passer ...", section "Optimisation pour le
+  Nemotron à mille milliards de paramètres").
 * ``fingerprint`` -- chunk-wise tensor fingerprint with a header over dtype,
   shape and numel (same French page, section "Méthodologie de débogage du
   non-déterminisme": fingerprints computed on the GPU with shape, dtype and
@@ -100,6 +106,8 @@ def _load():
         lib.oracle_expert_rows.restype = ci
         lib.oracle_dprob_from_output.argtypes = [P, P, P, i64, ci, ci, P, i64, ci, P, P]
         lib.oracle_dprob_from_output.restype = None
+        lib.oracle_wgrad_entries.argtypes = [P, P, P, ci, ci, ci, P, i64, P]
+        lib.oracle_wgrad_entries.restype = None
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = ci
         _lib = lib
@@ -222,6 +230,35 @@ def full(inputs, slot_width=SLOT_WIDTH):
                               slot_width=slot_width)
     dprob = combine(D, row_src, cfg.T, cfg.topk)
     return dict(off=off, row_src=row_src, Y=Y, Yb=Yb, P=P, D=D, dprob=dprob)
+
+
+# --------------------------------------------------------------------------
+# weight gradient of the grouped GEMM
+# --------------------------------------------------------------------------
+def wgrad_entries(X, dY, off, entries):
+    """dW[e, n, c] = sum over the expert's rows r (ascending) of dY[r, n] * X[r, c],
+    binary64 (C), for each (e, n, c) row of `entries` [m, 3]."""
+    X = np.ascontiguousarray(X, dtype=np.uint16)
+    dY = np.ascontiguousarray(dY, dtype=np.uint16)
+    off = np.ascontiguousarray(off, dtype=np.int32)
+    ent = np.ascontiguousarray(entries, dtype=np.int64).reshape(-1, 3)
+    R, K = X.shape
+    R2, N = dY.shape
+    E = off.size - 1
+    assert R2 == R and int(off[-1]) == R
+    if ent.size and (ent[:, 0].min() < 0 or ent[:, 0].max() >= E or ent[:, 1].max() >= N or ent[:, 2].max() >= K):
+        raise ValueError("entry out of range")
+    out = np.empty(ent.shape[0], dtype=np.float64)
+    _load().oracle_wgrad_entries(_ptr(X), _ptr(dY), _ptr(off), E, K, N, _ptr(ent), ent.shape[0], _ptr(out))
+    return out
+
+
+def wgrad_expert(X, dY, off, e):
+    """The whole dW[e] [N, K] (binary64) by the same definition."""
+    N, K = np.asarray(dY).shape[1], np.asarray(X).shape[1]
+    n, c = np.meshgrid(np.arange(N), np.arange(K), indexing="ij")
+    ent = np.stack([np.full(N * K, e), n.ravel(), c.ravel()], axis=1)
+    return wgrad_entries(X, dY, off, ent).reshape(N, K)
 
 
 # --------------------------------------------------------------------------

@@ -11,6 +11,7 @@
  *   Yb[r,n]  = bf16_rne(Y[r,n])                             stored output
  *   P[s,r]   = sum_{n in slot s} G[t(r),n] * Yb[r,n]        private slot partial
  *   D[r]     = sum_{n=0..N-1} G[t(r),n] * Yb[r,n]           dprob of row r
+ *   dW[e,n,c] = sum_{r in expert e} dY[r,n] * X[r,c]        weight gradient
  *
  * where e(r) is the expert whose row range [off[e], off[e+1]) holds r, and
  * t(r) = row_src[r] / topk is the token the permuted row came from.
@@ -196,6 +197,28 @@ void oracle_dprob_from_output(const uint16_t* G, const uint16_t* expert_out,
                 d += bf16_value(g[n]) * bf16_value(y[n]);
             D[i] = d;
         }
+    }
+}
+
+/*
+ * Weight gradient of the grouped GEMM (the FFN-out projection's wgrad): for
+ * each requested entry (e, n, c) = ent[3i], ent[3i+1], ent[3i+2],
+ *   dW[e, n, c] = sum_{r = off[e]} ^ {off[e+1]-1} dY[r, n] * X[r, c]
+ * in binary64, rows ascending; an expert without rows gives 0.
+ * X: [R,K] bf16 bits (the GEMM's input rows), dY: [R,N] bf16 bits (gradient
+ * at expert_out), off: [E+1].
+ */
+void oracle_wgrad_entries(const uint16_t* X, const uint16_t* dY, const int32_t* off, int E, int K, int N,
+                          const int64_t* ent, int64_t nent, double* out)
+{
+    (void)E;
+#pragma omp parallel for schedule(dynamic, 64)
+    for (int64_t i = 0; i < nent; ++i) {
+        int64_t e = ent[3 * i], n = ent[3 * i + 1], c = ent[3 * i + 2];
+        double acc = 0.0;
+        for (int64_t r = off[e]; r < off[e + 1]; ++r)
+            acc += bf16_value(dY[r * (int64_t)N + n]) * bf16_value(X[r * (int64_t)K + c]);
+        out[i] = acc;
     }
 }
 
