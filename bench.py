@@ -247,6 +247,26 @@ def dispatch_combine(api, cfg, inp, src, row_of, expert_out, timed, dev, iters):
     return res
 
 
+def wgrad_measure(api, cfg, X, dY, off, ws, timed, dev, iters):
+    """The deterministic weight gradient dW[e] = dY_e^T X_e (fp32 [E, N, K]) on the
+    step's X_perm and, as dY, its expert_out rows.  Algorithmic bytes: X and dY
+    read once (R*K*2 + R*N*2) and dW written once (E*N*K*4); flops 2*R*K*N."""
+    import torch
+    pk, _ = peaks()
+    dW = torch.empty(cfg.E, cfg.N, cfg.K, dtype=torch.float32, device=dev)
+    ms = timed(lambda: api.grouped_gemm_wgrad(X, dY, off, ws, dW=dW), iters)
+    if api.read_status(ws) != 0:
+        raise RuntimeError("device status set while timing the weight gradient")
+    b = cfg.R * cfg.K * 2 + cfg.R * cfg.N * 2 + cfg.E * cfg.N * cfg.K * 4 + (cfg.E + 1) * 4
+    flops = 2.0 * cfg.R * cfg.K * cfg.N
+    gbs = b / (ms * 1e-3) / 1e9
+    del dW
+    torch.cuda.empty_cache()
+    return {"ms": ms, "tflops": flops / (ms * 1e-3) / 1e12, "algorithmic_bytes": b, "achieved_gbs": gbs,
+            "peak_gbs": pk["hbm_gbs"], "frac": gbs / pk["hbm_gbs"], "bound": "hbm",
+            "tensor_frac": flops / (ms * 1e-3) / 1e12 / pk["bf16_tflops"]}
+
+
 # ---------------------------------------------------------------------------
 def run_ours(args):
     import torch
@@ -393,6 +413,7 @@ def run_ours(args):
     # ---------------- the steps either side of the GEMM (not in the step)
     around = None if args.skip_dispatch else dispatch_combine(api, cfg, inp, src, row_of, out, timed, dev,
                                                               args.tax_iters)
+    wg = None if args.skip_wgrad else wgrad_measure(api, cfg, X, out, off, ws, timed, dev, args.tax_iters)
 
     # ---------------- end to end through the public API, host buffers
     e2e = None
@@ -464,6 +485,7 @@ def run_ours(args):
         "roofline": roof,
         "determinism_tax": tax,
         "dispatch_combine": around,
+        "wgrad": wg,
         "e2e": e2e,
         "clocks": clocks,
     }
@@ -490,6 +512,7 @@ def main():
     ap.add_argument("--skip-imbal", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-dispatch", action="store_true")
+    ap.add_argument("--skip-wgrad", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

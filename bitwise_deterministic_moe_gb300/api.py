@@ -79,6 +79,7 @@ def load() -> ctypes.CDLL:
         "moe_grouped_gemm_dprob": ([P, P, P, I, I, I, I, P, P, P, I, I, P, P, LP, P, SZ, P], I),
         "moe_grouped_gemm_dprob_atomic": ([P, P, P, I, I, I, I, P, P, P, I, I, P, LP, P, SZ, P], I),
         "moe_grouped_gemm_dprob_serial": ([P, P, P, I, I, I, I, P, P, P, I, I, P, LP, P, SZ, P], I),
+        "moe_grouped_gemm_wgrad": ([P, P, P, I, I, I, I, P, I, LP, P, SZ, P], I),
         "moe_dprob_epilogue": ([P, P, P, P, I, I, I, I, I, P, P], I),
         "moe_dprob_combine": ([P, P, I, I, I, I, P, P], I),
         "dmoe_fingerprint_num_chunks": ([SZ, SZ], SZ),
@@ -291,6 +292,29 @@ def grouped_gemm_dprob_serial(X_perm, W, expert_offsets, grad_out, row_src, topk
                                               _launch(num_ctas, flags), _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "moe_grouped_gemm_dprob_serial")
     return out, dprob
+
+
+def grouped_gemm_wgrad(X_perm, dY, expert_offsets, ws, dW=None, E: Optional[int] = None, accumulate: bool = False,
+                       num_ctas: int = 0, stream=None):
+    """Deterministic weight gradient dW[e] (+)= dY_e^T X_e: fp32 [E, N, K]."""
+    _need(X_perm, torch.bfloat16, "X_perm")
+    _need(dY, torch.bfloat16, "dY")
+    _need(expert_offsets, torch.int32, "expert_offsets")
+    R, K = X_perm.shape
+    R2, N = dY.shape
+    if R2 != R:
+        raise ValueError("X_perm and dY must have the same rows")
+    E = expert_offsets.numel() - 1 if E is None else E
+    if dW is None:
+        if accumulate:
+            raise ValueError("accumulate needs an existing dW")
+        dW = torch.empty(E, N, K, dtype=torch.float32, device=X_perm.device)
+    _need(dW, torch.float32, "dW", (E, N, K))
+    st = load().moe_grouped_gemm_wgrad(_ptr(X_perm), _ptr(dY), _ptr(expert_offsets), R, E, K, N, _ptr(dW),
+                                       1 if accumulate else 0, _launch(num_ctas), _ptr(ws), ws.numel(),
+                                       _stream(stream))
+    _check(st, "moe_grouped_gemm_wgrad")
+    return dW
 
 
 def dprob_epilogue(grad_out, expert_out, expert_offsets, row_src, topk: int, slots=None, stream=None):

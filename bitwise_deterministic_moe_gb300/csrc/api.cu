@@ -258,6 +258,29 @@ dmoe_status moe_grouped_gemm_dprob_serial(const void* X_perm, const void* W, con
   return cuda_status(launch_grouped_gemm(GemmMode::kSerial, a, s));
 }
 
+dmoe_status moe_grouped_gemm_wgrad(const void* X_perm, const void* dY, const int32_t* expert_offsets, int R, int E,
+                                   int K, int N, float* dW, int accumulate, const dmoe_launch* launch, void* ws,
+                                   size_t ws_bytes, dmoe_stream_t stream) {
+  if (!expert_offsets || !dW || R < 0 || E < 1 || K < 1 || N < 1) return DMOE_ERR_INVALID_ARG;
+  if (R > 0 && (!X_perm || !dY)) return DMOE_ERR_INVALID_ARG;
+  if (!aligned16(X_perm) || !aligned16(dY) || !aligned16(dW)) return DMOE_ERR_INVALID_ARG;
+  if (accumulate != 0 && accumulate != 1) return DMOE_ERR_INVALID_ARG;
+  if (E > DMOE_MAX_EXPERTS || K % 8 != 0 || K > 65536 || N % DMOE_SLOT_COLS != 0 || N > 65536)
+    return DMOE_ERR_UNSUPPORTED;
+  if ((long long)E * N >= (1ll << 31)) return DMOE_ERR_UNSUPPORTED;
+  if (!ws || ws_bytes < DMOE_WS_STATUS_BYTES) return DMOE_ERR_WORKSPACE;
+  WgradArgs a{};
+  a.X = X_perm; a.dY = dY; a.offsets = expert_offsets;
+  a.R = R; a.E = E; a.K = K; a.N = N;
+  a.dW = dW;
+  a.accumulate = accumulate;
+  a.status = status_ptr(ws);
+  a.sched = sched_ptr(ws);
+  a.num_ctas = launch ? launch->num_ctas : 0;
+  if (a.num_ctas < 0) return DMOE_ERR_INVALID_ARG;
+  return cuda_status(launch_grouped_wgrad(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 dmoe_status moe_dprob_epilogue(const void* grad_out, const void* expert_out, const int32_t* expert_offsets,
                                const int32_t* row_src, int R, int E, int T, int topk, int N, float* slots,
                                dmoe_stream_t stream) {

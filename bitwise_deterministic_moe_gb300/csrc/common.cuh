@@ -190,6 +190,12 @@ __device__ __forceinline__ bool counter_wait(const int* ctr, int target, volatil
   }
 }
 
+// Makes this thread's generic-proxy shared-memory writes visible to the async
+// proxy (TMA, tensor-core operand reads) once ordered by a later barrier.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }

@@ -33,6 +33,20 @@ struct GemmArgs {
 cudaError_t launch_grouped_gemm(GemmMode mode, const GemmArgs& a, cudaStream_t stream);       // CTA pairs
 cudaError_t launch_grouped_gemm_1sm(GemmMode mode, const GemmArgs& a, cudaStream_t stream);   // single CTAs
 
+// grouped-GEMM weight gradient: dW[e] (+)= dY_e^T X_e
+struct WgradArgs {
+  const void* X;              // bf16 [R, K]
+  const void* dY;             // bf16 [R, N]
+  const int32_t* offsets;     // [E+1]
+  int R, E, K, N;
+  float* dW;                  // fp32 [E, N, K]
+  int accumulate;             // 0: overwrite, 1: add to the existing values
+  int* status;
+  int* sched;
+  int num_ctas;
+};
+cudaError_t launch_grouped_wgrad(const WgradArgs& a, cudaStream_t stream);
+
 // serialized-writer control: bytes of its per-(m-tile, row quarter) counters
 size_t serial_flag_bytes(long long R, int E);
 

@@ -228,6 +228,30 @@ dmoe_status moe_grouped_gemm_dprob_atomic(const void* X_perm, const void* W, con
                                           dmoe_stream_t stream);
 
 /*
+ * Grouped-GEMM weight gradient (the FFN-out projection's wgrad), deterministic:
+ *     dW[e, n, c] = sum over rows r in [off[e], off[e+1]) of dY[r, n] * X_perm[r, c]
+ * (accumulate = 1: dW[e, n, c] += that sum, one fp32 addition per element).
+ * A weight-gradient path is one of the workloads whose determinism overhead
+ * the pages measure ("Trillion-Parameter Pretraining ...", section
+ * "Synopsis").  Every 128 x 256 output tile is reduced by one CTA over all of
+ * its expert's rows, in ascending blocks of 64 rows, with fp32 accumulation on
+ * the tensor cores: there are no split-K partials and no atomics, so the bits
+ * do not depend on num_ctas, the stream or the schedule.  An expert without
+ * rows gets dW[e] = 0 (unchanged when accumulating).
+ *   X_perm          bf16 [R, K]      the forward GEMM's input rows
+ *   dY              bf16 [R, N]      gradient at expert_out, same row order
+ *   expert_offsets  int32 [E+1]      a partition of [0, R); otherwise
+ *                                    DMOE_ERR_ROUTING and dW is left unwritten
+ *   dW              fp32 [E, N, K]   out (16-byte aligned)
+ * Shapes as for the forward GEMM: N % 128 == 0, K % 8 == 0, both <= 65536,
+ * 1 <= E <= DMOE_MAX_EXPERTS.  launch->flags is ignored.
+ */
+dmoe_status moe_grouped_gemm_wgrad(const void* X_perm, const void* dY, const int32_t* expert_offsets,
+                                   int R, int E, int K, int N, float* dW, int accumulate,
+                                   const dmoe_launch* launch, void* ws, size_t ws_bytes,
+                                   dmoe_stream_t stream);
+
+/*
  * The serialized-writer control: deterministic without private slots.  The
  * same GEMM and per-slot partials, but the writers of one row take turns:
  * slot s of a block of 32 rows is added into dprob only after slots

@@ -1,0 +1,171 @@
+"""Deterministic grouped-GEMM weight gradient on the GPU vs the oracle.
+
+dW[e] = dY_e^T X_e over each expert's rows, fp32 on the tensor cores with one
+CTA per output tile, compared element by element with the binary64 oracle:
+within rel 2e-3 of each expert's max |dW| (the fp32 bar used for dprob) and
+within a per-element bound from the arithmetic, (rows + 16) * 2^-23 times
+sum_r |dY[r, n] X[r, c]| (an fp32 accumulation chain over the expert's rows).
+Shapes span partial column tiles (K % 256 != 0, boxes past K), ragged row
+blocks (the rows past an expert's end are zeroed in shared memory), empty
+experts, many small experts, and the full LatentMoE-shaped size.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from bitwise_deterministic_moe_gb300 import api, synth
+from tests import gpu_util
+from tests.gpu_util import bf16_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    gpu_util.ensure_built()
+
+
+class WProblem:
+    def __init__(self, cfg, ids=None):
+        self.cfg = cfg
+        inp = synth.make_inputs(cfg, with_weights=False)
+        self.ids_np = inp.topk_ids if ids is None else ids
+        self.off_np, _ = oracle.routing(self.ids_np, cfg.E)
+        self.X_np = inp.X
+        self.dY_np = synth._normal_bf16(cfg.seed, 11, (cfg.R, cfg.N), 0.1)
+        self.X = bf16_dev(self.X_np)
+        self.dY = bf16_dev(self.dY_np)
+        self.off = torch.from_numpy(self.off_np).cuda()
+        self.ws = api.workspace(cfg.T, cfg.topk, cfg.E)
+
+    def run(self, **kw):
+        return api.grouped_gemm_wgrad(self.X, self.dY, self.off, self.ws, **kw)
+
+    def check(self, dW, ent):
+        """Compare the (e, n, c) entries of dW with the oracle."""
+        ent = np.asarray(ent, dtype=np.int64).reshape(-1, 3)
+        ref = oracle.wgrad_entries(self.X_np, self.dY_np, self.off_np, ent)
+        mag = oracle.wgrad_entries(self.X_np & 0x7FFF, self.dY_np & 0x7FFF, self.off_np, ent)
+        idx = torch.from_numpy((ent[:, 0] * self.cfg.N + ent[:, 1]) * self.cfg.K + ent[:, 2]).cuda()
+        got = dW.reshape(-1).index_select(0, idx).double().cpu().numpy()
+        rows = np.diff(self.off_np)[ent[:, 0]]
+        bound = (rows + 16) * 2.0 ** -23 * mag
+        assert (np.abs(got - ref) <= bound + 1e-30).all(), float(np.max(np.abs(got - ref) / (mag + 1e-30)))
+        for e in np.unique(ent[:, 0]):
+            m = ent[:, 0] == e
+            scale = np.abs(ref[m]).max()
+            assert np.abs(got[m] - ref[m]).max() <= 2e-3 * scale + 1e-30
+        return float(np.max(np.abs(got - ref) / (mag + 1e-30)))
+
+
+def all_entries(cfg):
+    e, n, c = np.meshgrid(np.arange(cfg.E), np.arange(cfg.N), np.arange(cfg.K), indexing="ij")
+    return np.stack([e.ravel(), n.ravel(), c.ravel()], axis=1)
+
+
+def sampled_entries(cfg, off, m, seed):
+    rng = np.random.default_rng(seed)
+    e = rng.integers(0, cfg.E, m)
+    hot = int(np.argmax(np.diff(off)))
+    e[: m // 8] = hot                                     # the heaviest expert, always
+    n = rng.integers(0, cfg.N, m)
+    c = rng.integers(0, cfg.K, m)
+    c[: m // 16] = cfg.K - 1 - rng.integers(0, min(8, cfg.K), m // 16)   # the last columns
+    return np.stack([e, n, c], axis=1)
+
+
+SHAPES = [
+    synth.CONFIGS["tiny"],
+    synth.custom_config("ragged", T=600, E=12, topk=3, K=320, N=384, index=301),   # column tile 2 of 2 partial
+    synth.custom_config("wide", T=300, E=5, topk=2, K=72, N=1024, index=302),      # K < one box pair
+    synth.custom_config("zipf", T=1024, E=64, topk=6, K=256, N=512, routing="zipf", index=304),
+]
+
+
+@pytest.mark.parametrize("cfg", SHAPES, ids=[c.name for c in SHAPES])
+def test_wgrad_parity(cfg):
+    prob = WProblem(cfg)
+    dW = prob.run()
+    assert api.read_status(prob.ws) == 0
+    ent = all_entries(cfg) if cfg.E * cfg.N * cfg.K <= 2_000_000 else sampled_entries(cfg, prob.off_np, 200_000, 1)
+    prob.check(dW, ent)
+
+
+def test_wgrad_many_small_experts_and_holes():
+    cfg = synth.custom_config("manyexp", T=700, E=1024, topk=8, K=128, N=256, index=303)
+    inp = synth.make_inputs(cfg, with_weights=False)
+    ids = inp.topk_ids.copy()
+    ids[ids % 7 == 0] = 1                          # empty experts 0, 7, 14, ...; expert 1 heavy
+    prob = WProblem(cfg, ids)
+    sentinel = torch.full((cfg.E, cfg.N, cfg.K), 7.0, dtype=torch.float32, device="cuda")
+    dW = prob.run(dW=sentinel)
+    assert api.read_status(prob.ws) == 0
+    counts = np.diff(prob.off_np)
+    empty = np.flatnonzero(counts == 0)
+    assert empty.size > 0 and torch.count_nonzero(dW[torch.from_numpy(empty).cuda()]).item() == 0
+    prob.check(dW, sampled_entries(cfg, prob.off_np, 100_000, 2))
+
+
+@pytest.mark.parametrize("cfg", [SHAPES[1], SHAPES[3]], ids=["ragged", "zipf"])
+def test_wgrad_bitwise_across_grids_and_streams(cfg):
+    prob = WProblem(cfg)
+    ref = prob.run().clone()
+    for n in (37, 1, 0):
+        assert torch.equal(prob.run(num_ctas=n).view(torch.int32), ref.view(torch.int32))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = [torch.empty_like(ref) for _ in streams]
+    wss = [api.workspace(cfg.T, cfg.topk, cfg.E) for _ in streams]
+    torch.cuda.synchronize()
+    for it in range(5):
+        for s, o, w in zip(streams, outs, wss):
+            with torch.cuda.stream(s):
+                api.grouped_gemm_wgrad(prob.X, prob.dY, prob.off, w, dW=o)
+        torch.cuda.synchronize()
+        for o in outs:
+            assert torch.equal(o.view(torch.int32), ref.view(torch.int32))
+
+
+def test_wgrad_accumulate_is_one_fp32_add():
+    cfg = SHAPES[1]
+    prob = WProblem(cfg)
+    fresh = prob.run().clone()
+    base = torch.randn(cfg.E, cfg.N, cfg.K, device="cuda")
+    acc = base.clone()
+    prob.run(dW=acc, accumulate=True)
+    assert api.read_status(prob.ws) == 0
+    assert torch.equal(acc.view(torch.int32), (base + fresh).view(torch.int32))
+
+
+def test_wgrad_bad_offsets_reported_and_nothing_written():
+    cfg = SHAPES[0]
+    prob = WProblem(cfg)
+    bad = prob.off.clone()
+    bad[2] = bad[3] + 1
+    sentinel = torch.full((cfg.E, cfg.N, cfg.K), 3.0, device="cuda")
+    api.grouped_gemm_wgrad(prob.X, prob.dY, bad, prob.ws, dW=sentinel)
+    assert api.read_status(prob.ws) == 3
+    assert bool((sentinel == 3.0).all())
+    prob.run()
+    assert api.read_status(prob.ws) == 0
+
+
+def test_wgrad_zero_rows():
+    ws = api.workspace(0, 2, 4)
+    X = torch.empty(0, 64, dtype=torch.bfloat16, device="cuda")
+    dY = torch.empty(0, 128, dtype=torch.bfloat16, device="cuda")
+    off = torch.zeros(5, dtype=torch.int32, device="cuda")
+    dW = torch.full((4, 128, 64), 5.0, device="cuda")
+    api.grouped_gemm_wgrad(X, dY, off, ws, dW=dW)
+    assert bool((dW == 0).all())
+
+
+@pytest.mark.parametrize("name", ["latent", "imbal"])
+def test_wgrad_full_size_sampled(name):
+    cfg = synth.CONFIGS[name]
+    prob = WProblem(cfg)
+    dW = prob.run()
+    assert api.read_status(prob.ws) == 0
+    prob.check(dW, sampled_entries(cfg, prob.off_np, 4000, 3))
+    again = prob.run(num_ctas=77)
+    assert torch.equal(again.view(torch.int32), dW.view(torch.int32))
