@@ -23,12 +23,12 @@
 // Design (one CTA per SM, persistent, warp-specialised, 320 threads):
 //   warp 0     TMA producer: per stage dY [64 r x 128 n] and X [64 r x 256 c].
 //   warp 1     tcgen05.mma issuer (lane 0): 128x256x16 MMAs, fp32 in tensor
-//              memory (2 x 256 columns).  The whole warp zeroes the rows past
-//              the expert's end in a tile's last stage before its MMAs (those
-//              rows belong to the next expert), so no row is ever counted twice.
+//              memory (2 x 256 columns).  In a tile's last stage only the
+//              16-row steps holding the expert's rows are issued, and the whole
+//              warp first zeroes the rows of the last step that belong to the
+//              next expert, so no row is ever counted twice.
 //   warps 2-9  epilogue: tensor memory -> registers -> swizzled shared memory ->
-//              coalesced 16-byte stores of dW rows (plus the old value in
-//              accumulate mode).
+//              TMA tensor stores of dW (add-reduce stores in accumulate mode).
 // Tiles (one 128 x 256 block of one expert's dW) of experts with many rows come
 // first, then the rest, each class in expert order, handed out dynamically.
 #include <cuda.h>
@@ -39,6 +39,7 @@
 namespace dmoe {
 
 bool make_tmap_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows);
+bool make_tmap_f32_store(CUtensorMap* m, void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows);
 
 namespace {
 
@@ -135,7 +136,7 @@ __device__ __forceinline__ Tile decode_tile(int t, const Ctrl& c, int E, int NTn
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_wgrad_kernel(const __grid_constant__ CUtensorMap tmap_dy, const __grid_constant__ CUtensorMap tmap_x,
-                     const KParams p) {
+                     const __grid_constant__ CUtensorMap tmap_dw, const KParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Ctrl& c = *reinterpret_cast<Ctrl*>(base + size_t(STAGES) * STAGE_BYTES + size_t(EPI_WARPS) * STG_BYTES);
@@ -165,6 +166,7 @@ grouped_wgrad_kernel(const __grid_constant__ CUtensorMap tmap_dy, const __grid_c
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmap_dy);
     tma_prefetch_desc(&tmap_x);
+    tma_prefetch_desc(&tmap_dw);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&c.tmem_base), TMEM_COLS);
@@ -237,7 +239,8 @@ grouped_wgrad_kernel(const __grid_constant__ CUtensorMap tmap_dy, const __grid_c
           const int y = tl.row0 + kb * BK;   // rows past R are filled with zeros by the TMA unit
           mbar_arrive_expect_tx(full, STAGE_BYTES);
 #pragma unroll
-          for (int b = 0; b < BM / 64; ++b) tma_load_2d(sa + b * BOX_BYTES, &tmap_dy, full, tl.n0 + b * 64, y);
+          for (int b = 0; b < BM / 64; ++b)
+            tma_load_2d(sa + b * BOX_BYTES, &tmap_dy, full, tl.n0 + b * 64, y);
 #pragma unroll
           for (int b = 0; b < BN / 64; ++b)   // boxes at c >= K are filled with zeros
             tma_load_2d(sa + A_STAGE_BYTES + b * BOX_BYTES, &tmap_x, full, tl.c0 + b * 64, y);
@@ -275,12 +278,15 @@ grouped_wgrad_kernel(const __grid_constant__ CUtensorMap tmap_dy, const __grid_c
       for (int kb = 0; kb < KB; ++kb) {
         if (!warp_wait(smem_u32(&c.full[stage]), ph, &c.abort, p.status, lane, p.wait_ns)) { ok = false; break; }
         const uint32_t sa = stage0 + stage * STAGE_BYTES;
-        const int valid = tl.rows - kb * BK;
-        if (valid < BK) {
-          // Rows valid..63 of this block belong to the next expert (or lie past
-          // R): zero them in every box.  A row is one 128-byte line of a box
-          // (the swizzle only permutes 16-byte pieces inside the line).
-          const int words = (BK - valid) * 8;
+        const int valid = min(tl.rows - kb * BK, BK);
+        const int groups = (valid + UMMA_K - 1) / UMMA_K;   // 16-row MMA steps holding the expert's rows
+        const int pad_end = groups * UMMA_K;
+        if (valid < pad_end) {
+          // Rows valid..pad_end-1 of the last 16-row step belong to the next
+          // expert (or lie past R): zero them in every box (a row is one
+          // 128-byte line of a box; the swizzle only permutes 16-byte pieces
+          // inside it).  Steps past pad_end are not issued at all.
+          const int words = (pad_end - valid) * 8;
           for (int i = lane; i < BOXES * words; i += 32) {
             const int b = i / words;
             const int w = i - b * words;
@@ -293,8 +299,7 @@ grouped_wgrad_kernel(const __grid_constant__ CUtensorMap tmap_dy, const __grid_c
           tc_fence_after();
           const uint64_t adesc = smem_desc_mn128(sa);
           const uint64_t bdesc = smem_desc_mn128(sa + A_STAGE_BYTES);
-#pragma unroll
-          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+          for (int kk = 0; kk < groups; ++kk) {
             // 16 rows = two 8-row groups = 2 KB further along the reduction
             tc_mma_f16(d_tmem, adesc + uint64_t(kk * 128), bdesc + uint64_t(kk * 128), kIdesc,
                        (kb | kk) != 0 ? 1u : 0u);
@@ -319,11 +324,14 @@ grouped_wgrad_kernel(const __grid_constant__ CUtensorMap tmap_dy, const __grid_c
     // -------------------------------------------------- epilogue (8 warps)
     // Warp w reads TMEM lanes 32*(w%4)..+31 (dW rows n0 + 32q ..); warps 2-5
     // take columns 0..127 of the tile, warps 6-9 columns 128..255.  Each
-    // 32-row x 16-column fp32 piece goes through a 2 KB swizzled staging buffer
-    // so that four lanes write 64 contiguous bytes of a dW row.
+    // 32-row x 16-column fp32 piece is written to a 2 KB staging buffer in the
+    // TMA unit's 64-byte-swizzled layout (piece kk of row r at kk ^ ((r/2)%4),
+    // which also keeps the shared-memory writes free of bank conflicts) and
+    // sent to dW by one TMA tensor store -- an add-reduce in accumulate mode,
+    // one fp32 addition per element.  Columns past K are clipped by the TMA
+    // unit.
     const int q = warp & 3;
     const int h = (warp - EPI_WARP0) / 4;
-    const int k4 = lane & 3;
     const uint32_t stg = stage0 + uint32_t(STAGES * STAGE_BYTES + (warp - EPI_WARP0) * STG_BYTES);
     int acc = 0;
     uint32_t aph = 0;
@@ -350,6 +358,7 @@ grouped_wgrad_kernel(const __grid_constant__ CUtensorMap tmap_dy, const __grid_c
       if (!warp_wait(smem_u32(&c.acc_full[acc]), aph, &c.abort, p.status, lane, p.wait_ns)) break;
       tc_fence_after();
       const uint32_t tcol = tmem_base + uint32_t(acc * BN + h * 128) + (uint32_t(q * 32) << 16);
+      const int grow = tl.e * p.N + tl.n0 + q * 32;   // row of dW viewed as [E*N, K]
 #pragma unroll 1
       for (int ch = 0; ch < 4; ++ch) {
         uint32_t v[32];
@@ -357,32 +366,24 @@ grouped_wgrad_kernel(const __grid_constant__ CUtensorMap tmap_dy, const __grid_c
         tmem_wait_ld();
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-          // row `lane`, 16 columns -> four 16-byte pieces, piece kk at kk ^ ((lane >> 1) & 3)
+          const int cc = col0 + ch * 32 + half * 16;
+          if (lane == 0) bulk_wait_group_read<0>();   // the previous box has left the staging buffer
+          __syncwarp();
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const int j = half * 16 + kk * 4;
             sts_v4(stg + uint32_t(lane * 64 + ((kk ^ ((lane >> 1) & 3)) << 4)),
                    make_uint4(v[j], v[j + 1], v[j + 2], v[j + 3]));
           }
+          fence_proxy_async_smem();
           __syncwarp();
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int row = i * 8 + (lane >> 2);
-            uint4 val = lds_v4(stg + uint32_t(row * 64 + ((k4 ^ ((row >> 1) & 3)) << 4)));
-            const int cc = col0 + ch * 32 + half * 16 + k4 * 4;
-            if (cc < p.K) {
-              float* dst = dw_rows + size_t(row) * p.K + cc;
-              if (p.accumulate) {
-                const float4 old = *reinterpret_cast<const float4*>(dst);
-                val.x = __float_as_uint(__fadd_rn(old.x, __uint_as_float(val.x)));
-                val.y = __float_as_uint(__fadd_rn(old.y, __uint_as_float(val.y)));
-                val.z = __float_as_uint(__fadd_rn(old.z, __uint_as_float(val.z)));
-                val.w = __float_as_uint(__fadd_rn(old.w, __uint_as_float(val.w)));
-              }
-              stg_v4(dst, val);
-            }
+          if (lane == 0 && cc < p.K) {
+            if (p.accumulate)
+              tma_reduce_add_2d(&tmap_dw, stg, cc, grow);
+            else
+              tma_store_2d(&tmap_dw, stg, cc, grow);
+            bulk_commit_group();
           }
-          __syncwarp();
         }
       }
       tc_fence_before();
@@ -390,6 +391,8 @@ grouped_wgrad_kernel(const __grid_constant__ CUtensorMap tmap_dy, const __grid_c
       if (lane == 0) mbar_arrive(smem_u32(&c.acc_empty[acc]));
       if (++acc == ACC_BUFS) { acc = 0; aph ^= 1u; }
     }
+    if (lane == 0) bulk_wait_group_all();   // every store has landed before the CTA exits
+    __syncwarp();
   }
 
   __syncthreads();
@@ -415,9 +418,10 @@ cudaError_t launch_grouped_wgrad(const WgradArgs& a, cudaStream_t stream) {
   if (a.R == 0) {   // no rows anywhere: every dW[e] is zero
     return a.accumulate ? cudaSuccess : cudaMemsetAsync(a.dW, 0, dw_bytes, stream);
   }
-  CUtensorMap tdy, tx;
+  CUtensorMap tdy, tx, tdw;
   if (!make_tmap_bf16(&tdy, a.dY, uint64_t(a.R), uint64_t(a.N), BK)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16(&tx, a.X, uint64_t(a.R), uint64_t(a.K), BK)) return cudaErrorInvalidValue;
+  if (!make_tmap_f32_store(&tdw, a.dW, uint64_t(a.E) * a.N, uint64_t(a.K), 32)) return cudaErrorInvalidValue;
   KParams kp;
   kp.offsets = a.offsets;
   kp.E = a.E;
@@ -440,7 +444,7 @@ cudaError_t launch_grouped_wgrad(const WgradArgs& a, cudaStream_t stream) {
     attr_done = true;
   }
   const int grid = a.num_ctas > 0 ? a.num_ctas : device_sm_count();
-  return launch_chained(grouped_wgrad_kernel, dim3(grid), dim3(NUM_THREADS), kSmemBytes, stream, tdy, tx, kp);
+  return launch_chained(grouped_wgrad_kernel, dim3(grid), dim3(NUM_THREADS), kSmemBytes, stream, tdy, tx, tdw, kp);
 }
 
 }  // namespace dmoe
