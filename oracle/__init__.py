@@ -35,6 +35,10 @@ Contents and the passage each part follows:
   overhead the pages measure ("Trillion-Parameter Pretraining ...", section
   "Synopsis"; "NVIDIA fait passer ...", section "Optimisation pour le
   Nemotron à mille milliards de paramètres").
+* ``mxfp8_quantize`` / ``nvfp4_quantize`` -- the block-scaled encodings whose
+  encoded values and scale buffers the pages fingerprint ("NVIDIA fait passer
+  ...", section "Méthodologie de débogage du non-déterminisme"); E4M3, E2M1
+  and E8M0 decoded and encoded from their format definitions.
 * ``fingerprint`` -- chunk-wise tensor fingerprint with a header over dtype,
   shape and numel (same French page, section "Méthodologie de débogage du
   non-déterminisme": fingerprints computed on the GPU with shape, dtype and
@@ -300,6 +304,127 @@ def token_combine(expert_out, probs, row_src, tokens=None):
     for j in range(topk):
         acc += probs[tokens, j].astype(np.float64)[:, None] * bf16_to_f64(Yb[row_of[tokens, j]])
     return acc, bf16_rne(acc)
+
+
+# --------------------------------------------------------------------------
+# block-scaled low-precision encodings (MXFP8, NVFP4)
+# --------------------------------------------------------------------------
+def e4m3_value(code) -> np.ndarray:
+    """binary64 value of FP8 E4M3 codes (1 sign, 4 exponent bits with bias 7,
+    3 fraction bits; exponent field 0 is subnormal, m/8 * 2^-6; S.1111.111 is
+    NaN; no infinities; largest finite 1.75 * 2^8 = 448)."""
+    c = np.asarray(code, dtype=np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    mag = np.where((c & 0x7F) == 0x7F, np.nan, mag)
+    return sign * mag
+
+
+def e2m1_value(code) -> np.ndarray:
+    """binary64 value of FP4 E2M1 codes (1 sign, 2 exponent bits with bias 1,
+    1 fraction bit): 0, 0.5, 1, 1.5, 2, 3, 4, 6 and their negatives."""
+    c = np.asarray(code, dtype=np.int64)
+    sign = np.where(c & 0x8, -1.0, 1.0)
+    e = (c >> 1) & 0x3
+    m = c & 0x1
+    mag = np.where(e == 0, m * 0.5, (1.0 + m / 2.0) * np.exp2(e - 1.0))
+    return sign * mag
+
+
+def _encode_rne_sat(x, codes_pos, values_pos, sign_bit):
+    """Nearest representable value (ties to the even code), magnitudes above
+    the largest finite value saturate to it; the sign is kept (-0 stays -0).
+    codes_pos / values_pos: the non-negative finite codes, values ascending."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    idx = np.searchsorted(values_pos, a, side="right") - 1           # largest value <= a
+    idx = np.clip(idx, 0, len(values_pos) - 1)
+    hi = np.clip(idx + 1, 0, len(values_pos) - 1)
+    lo_v, hi_v = values_pos[idx], values_pos[hi]
+    d_lo, d_hi = a - lo_v, hi_v - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (codes_pos[hi] % 2 == 0) & (hi != idx))
+    code = np.where(pick_hi, codes_pos[hi], codes_pos[idx])
+    code = np.where(a >= values_pos[-1], codes_pos[-1], code)           # saturate
+    neg = np.signbit(x)
+    return (code | np.where(neg, sign_bit, 0)).astype(np.uint8)
+
+
+_E4M3_CODES = np.arange(0x7F, dtype=np.int64)                            # 0x00..0x7E: non-negative finite
+_E4M3_VALS = e4m3_value(_E4M3_CODES)
+_E2M1_CODES = np.arange(8, dtype=np.int64)
+_E2M1_VALS = e2m1_value(_E2M1_CODES)
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """binary64 -> E4M3 code, round to nearest even, saturating at +-448."""
+    return _encode_rne_sat(x, _E4M3_CODES, _E4M3_VALS, 0x80)
+
+
+def e2m1_encode(x) -> np.ndarray:
+    """binary64 -> E2M1 code (low 4 bits), round to nearest even, saturating at +-6."""
+    return _encode_rne_sat(x, _E2M1_CODES, _E2M1_VALS, 0x8)
+
+
+MX_BLOCK = 32
+NV_BLOCK = 16
+
+
+def mxfp8_quantize(x_bits):
+    """MXFP8 (OCP Microscaling Formats v1.0): each run of 32 consecutive values
+    of a row shares one E8M0 scale X = 2^s with s = floor(log2(amax)) - 8 (8 =
+    the E4M3 maximum exponent), clamped to s >= -127; the elements are E4M3
+    codes of V/X (round to nearest even, saturating).  An all-zero block gets
+    s = -127.  A block holding a NaN or an infinity gets scale 0xFF (NaN) and
+    NaN elements (0x7F).
+    x_bits: bf16 bit patterns [rows, cols], cols % 32 == 0.
+    Returns (values uint8 [rows, cols], scales uint8 [rows, cols/32])."""
+    x = bf16_to_f64(x_bits)
+    rows, cols = x.shape
+    assert cols % MX_BLOCK == 0
+    blk = x.reshape(rows, cols // MX_BLOCK, MX_BLOCK)
+    finite = np.isfinite(blk).all(axis=2)
+    amax = np.where(finite, np.abs(np.where(np.isfinite(blk), blk, 0.0)).max(axis=2), 0.0)
+    _, ex = np.frexp(amax)                           # amax = f * 2^ex, f in [0.5, 1)
+    s = np.where(amax > 0, ex - 1 - 8, -127)
+    s = np.maximum(s, -127)
+    scales = np.where(finite, s + 127, 0xFF).astype(np.uint8)
+    scaled = np.where(finite[..., None], blk * np.exp2(-s.astype(np.float64))[..., None], 0.0)
+    vals = e4m3_encode(scaled)
+    vals = np.where(finite[..., None], vals, np.uint8(0x7F)).astype(np.uint8)
+    return vals.reshape(rows, cols), scales
+
+
+def nvfp4_quantize(x_bits):
+    """NVFP4 with two-level scaling, every step in binary32 in this order:
+      amax_t   = max |x| over the tensor (finite inputs)
+      S_enc    = 2688 / amax_t  (2688 = 448 * 6; 1 when amax_t == 0)
+      per run of 16 consecutive values of a row:
+        amax_b  = max |x| over the block
+        s_b     = E4M3( (amax_b / 6) * S_enc )      round to nearest even, saturating
+        q_i     = E2M1( (x_i * S_enc) / value(s_b) )  (q_i = 0 when s_b encodes 0)
+    Two E2M1 codes per byte, element 2i in the low nibble.
+    x_bits: bf16 bit patterns [rows, cols], cols % 16 == 0.
+    Returns (packed uint8 [rows, cols/2], scales uint8 [rows, cols/16], S_enc float32)."""
+    x32 = bf16_to_f64(x_bits).astype(np.float32)
+    rows, cols = x32.shape
+    assert cols % NV_BLOCK == 0
+    amax_t = np.float32(np.abs(x32).max()) if x32.size else np.float32(0)
+    s_enc = np.float32(1.0) if amax_t == 0 else np.float32(np.float32(2688.0) / amax_t)
+    blk = x32.reshape(rows, cols // NV_BLOCK, NV_BLOCK)
+    amax_b = np.abs(blk).max(axis=2)
+    dec = (amax_b / np.float32(6.0)).astype(np.float32)
+    dec = (dec * s_enc).astype(np.float32)
+    scales = e4m3_encode(dec.astype(np.float64))
+    sv = e4m3_value(scales).astype(np.float32)
+    t = (blk * s_enc).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = (t / sv[..., None]).astype(np.float32)
+    r = np.where(sv[..., None] == 0, np.float32(0), r)
+    q = e2m1_encode(r.astype(np.float64)).reshape(rows, cols)
+    packed = (q[:, 0::2] & 0xF) | ((q[:, 1::2] & 0xF) << 4)
+    return packed.astype(np.uint8), scales, s_enc
 
 
 # --------------------------------------------------------------------------
