@@ -267,6 +267,25 @@ def wgrad_measure(api, cfg, X, dY, off, ws, timed, dev, iters):
             "tensor_frac": flops / (ms * 1e-3) / 1e12 / pk["bf16_tflops"]}
 
 
+def quant_measure(api, X, ws, timed, iters):
+    """MXFP8 and NVFP4 encodings of the step's X_perm [R, K] bf16.  Algorithmic
+    bytes: MXFP8 reads X once and writes R*K codes + R*K/32 scales; NVFP4 reads X
+    twice (tensor maximum, then the blocks) and writes R*K/2 + R*K/16 bytes."""
+    pk, _ = peaks()
+    n = X.numel()
+    res = {}
+    ms = timed(lambda: api.quantize_mxfp8(X), iters)
+    b = n * 2 + n + n // 32
+    res["mxfp8"] = {"ms": ms, "algorithmic_bytes": b, "achieved_gbs": b / (ms * 1e-3) / 1e9}
+    ms = timed(lambda: api.quantize_nvfp4(X, ws), iters)
+    b = 2 * n * 2 + n // 2 + n // 16
+    res["nvfp4"] = {"ms": ms, "algorithmic_bytes": b, "achieved_gbs": b / (ms * 1e-3) / 1e9}
+    for v in res.values():
+        v["peak_gbs"] = pk["hbm_gbs"]
+        v["frac"] = v["achieved_gbs"] / pk["hbm_gbs"]
+    return res
+
+
 # ---------------------------------------------------------------------------
 def run_ours(args):
     import torch
@@ -414,6 +433,7 @@ def run_ours(args):
     around = None if args.skip_dispatch else dispatch_combine(api, cfg, inp, src, row_of, out, timed, dev,
                                                               args.tax_iters)
     wg = None if args.skip_wgrad else wgrad_measure(api, cfg, X, out, off, ws, timed, dev, args.tax_iters)
+    qz = None if args.skip_quant else quant_measure(api, X, ws, timed, args.tax_iters)
 
     # ---------------- end to end through the public API, host buffers
     e2e = None
@@ -486,6 +506,7 @@ def run_ours(args):
         "determinism_tax": tax,
         "dispatch_combine": around,
         "wgrad": wg,
+        "quantize": qz,
         "e2e": e2e,
         "clocks": clocks,
     }
@@ -513,6 +534,7 @@ def main():
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-dispatch", action="store_true")
     ap.add_argument("--skip-wgrad", action="store_true")
+    ap.add_argument("--skip-quant", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

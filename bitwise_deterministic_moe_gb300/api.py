@@ -80,6 +80,8 @@ def load() -> ctypes.CDLL:
         "moe_grouped_gemm_dprob_atomic": ([P, P, P, I, I, I, I, P, P, P, I, I, P, LP, P, SZ, P], I),
         "moe_grouped_gemm_dprob_serial": ([P, P, P, I, I, I, I, P, P, P, I, I, P, LP, P, SZ, P], I),
         "moe_grouped_gemm_wgrad": ([P, P, P, I, I, I, I, P, I, LP, P, SZ, P], I),
+        "dmoe_quantize_mxfp8": ([P, I, I, P, P, P], I),
+        "dmoe_quantize_nvfp4": ([P, I, I, P, P, P, P, SZ, P], I),
         "moe_dprob_epilogue": ([P, P, P, P, I, I, I, I, I, P, P], I),
         "moe_dprob_combine": ([P, P, I, I, I, I, P, P], I),
         "dmoe_fingerprint_num_chunks": ([SZ, SZ], SZ),
@@ -346,6 +348,44 @@ def dprob_combine(slots, row_src, topk: int, dprob=None, stream=None):
     st = load().moe_dprob_combine(_ptr(slots), _ptr(row_src), R, S, T, topk, _ptr(dprob), _stream(stream))
     _check(st, "moe_dprob_combine")
     return dprob
+
+
+# ------------------------------------------------------------------ block-scaled encodings
+def quantize_mxfp8(x: torch.Tensor, values=None, scales=None, stream=None):
+    """MXFP8 encoding of a bf16 [rows, cols] tensor: (E4M3 codes uint8 [rows, cols],
+    E8M0 scales uint8 [rows, cols/32])."""
+    _need(x, torch.bfloat16, "x")
+    rows, cols = x.shape
+    if values is None:
+        values = torch.empty(rows, cols, dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty(rows, cols // 32, dtype=torch.uint8, device=x.device)
+    _need(values, torch.uint8, "values", (rows, cols))
+    _need(scales, torch.uint8, "scales", (rows, cols // 32))
+    st = load().dmoe_quantize_mxfp8(_ptr(x), rows, cols, _ptr(values), _ptr(scales), _stream(stream))
+    _check(st, "dmoe_quantize_mxfp8")
+    return values, scales
+
+
+def quantize_nvfp4(x: torch.Tensor, ws: torch.Tensor, packed=None, scales=None, s_enc=None, stream=None):
+    """NVFP4 encoding of a bf16 [rows, cols] tensor: (packed E2M1 uint8 [rows, cols/2],
+    E4M3 scales uint8 [rows, cols/16], tensor scale fp32 [1])."""
+    _need(x, torch.bfloat16, "x")
+    rows, cols = x.shape
+    dev = x.device
+    if packed is None:
+        packed = torch.empty(rows, cols // 2, dtype=torch.uint8, device=dev)
+    if scales is None:
+        scales = torch.empty(rows, cols // 16, dtype=torch.uint8, device=dev)
+    if s_enc is None:
+        s_enc = torch.empty(1, dtype=torch.float32, device=dev)
+    _need(packed, torch.uint8, "packed", (rows, cols // 2))
+    _need(scales, torch.uint8, "scales", (rows, cols // 16))
+    _need(s_enc, torch.float32, "s_enc", (1,))
+    st = load().dmoe_quantize_nvfp4(_ptr(x), rows, cols, _ptr(packed), _ptr(scales), _ptr(s_enc), _ptr(ws),
+                                    ws.numel(), _stream(stream))
+    _check(st, "dmoe_quantize_nvfp4")
+    return packed, scales, s_enc
 
 
 # ------------------------------------------------------------------ fingerprint

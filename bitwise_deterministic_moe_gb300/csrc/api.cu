@@ -327,6 +327,29 @@ dmoe_status moe_token_combine(const void* expert_out, const float* probs, const 
                                           ws ? status_ptr(ws) : nullptr, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+dmoe_status dmoe_quantize_mxfp8(const void* x, int rows, int cols, uint8_t* values, uint8_t* scales,
+                                dmoe_stream_t stream) {
+  if (rows < 0 || cols < 0) return DMOE_ERR_INVALID_ARG;
+  if (cols % 32 != 0) return DMOE_ERR_UNSUPPORTED;
+  const long long n = (long long)rows * cols;
+  if (n > 0 && (!x || !values || !scales)) return DMOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(values)) return DMOE_ERR_INVALID_ARG;
+  return cuda_status(launch_quantize_mxfp8(x, n, values, scales, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+dmoe_status dmoe_quantize_nvfp4(const void* x, int rows, int cols, uint8_t* packed, uint8_t* scales, float* s_enc,
+                                void* ws, size_t ws_bytes, dmoe_stream_t stream) {
+  if (rows < 0 || cols < 0 || !s_enc) return DMOE_ERR_INVALID_ARG;
+  if (cols % 16 != 0) return DMOE_ERR_UNSUPPORTED;
+  const long long n = (long long)rows * cols;
+  if (n > 0 && (!x || !packed || !scales)) return DMOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || (reinterpret_cast<uintptr_t>(packed) & 7) != 0) return DMOE_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < DMOE_WS_STATUS_BYTES + 4) return DMOE_ERR_WORKSPACE;
+  unsigned int* scratch = reinterpret_cast<unsigned int*>(static_cast<char*>(ws) + DMOE_WS_STATUS_BYTES);
+  return cuda_status(
+      launch_quantize_nvfp4(x, n, packed, scales, s_enc, scratch, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 size_t dmoe_fingerprint_num_chunks(size_t nbytes, size_t chunk_bytes) {
   if (chunk_bytes == 0) return 0;
   return (nbytes + chunk_bytes - 1) / chunk_bytes;

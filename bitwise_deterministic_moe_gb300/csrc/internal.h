@@ -47,6 +47,11 @@ struct WgradArgs {
 };
 cudaError_t launch_grouped_wgrad(const WgradArgs& a, cudaStream_t stream);
 
+// block-scaled encodings (n = elements, a multiple of the block)
+cudaError_t launch_quantize_mxfp8(const void* x, long long n, void* vals, void* scales, cudaStream_t stream);
+cudaError_t launch_quantize_nvfp4(const void* x, long long n, void* packed, void* scales, float* s_enc,
+                                  unsigned int* amax_scratch, cudaStream_t stream);
+
 // serialized-writer control: bytes of its per-(m-tile, row quarter) counters
 size_t serial_flag_bytes(long long R, int E);
 

@@ -333,6 +333,44 @@ dmoe_status moe_dprob_combine(const float* slots, const int32_t* row_src, int R,
                               float* dprob, dmoe_stream_t stream);
 
 /*
+ * Block-scaled low-precision encodings of a bf16 tensor [rows, cols]: the
+ * MXFP8 / NVFP4 operand forms whose encoded values and scale buffers the pages
+ * fingerprint ("NVIDIA fait passer ...", section "Méthodologie de débogage du
+ * non-déterminisme").  Every byte is a function of its own block (and, for
+ * NVFP4, of the tensor maximum, an order-independent reduction), computed with
+ * round-to-nearest-even conversions, so the bytes are identical on every run;
+ * fingerprint them with dmoe_fingerprint (dtype DMOE_U8).  Inputs are finite
+ * bf16 values except where stated.
+ *
+ * MXFP8 (OCP Microscaling Formats v1.0): each run of 32 consecutive values of
+ * a row shares one E8M0 scale X = 2^s, s = floor(log2(amax)) - 8, clamped to
+ * s >= -127 (an all-zero block gets s = -127); elements are E4M3 codes of
+ * v / X, nearest even, saturating at +-448.  A block holding a NaN or an
+ * infinity gets scale 0xFF and elements 0x7F.
+ *   values  uint8 [rows, cols]       E4M3 codes (16-byte aligned)
+ *   scales  uint8 [rows, cols / 32]  biased exponents s + 127
+ * cols % 32 == 0; x 16-byte aligned.
+ */
+dmoe_status dmoe_quantize_mxfp8(const void* x, int rows, int cols, uint8_t* values, uint8_t* scales,
+                                dmoe_stream_t stream);
+
+/*
+ * NVFP4: 16-value blocks of E2M1 elements with an E4M3 block scale and an fp32
+ * tensor scale, every step in binary32 in this order:
+ *   S_enc = 2688 / max|x| over the tensor   (2688 = 448 * 6; 1 for an all-zero tensor)
+ *   s_b   = E4M3((amax_b / 6) * S_enc)      per block, nearest even, saturating
+ *   q_i   = E2M1((x_i * S_enc) / s_b)       nearest even, saturating at +-6; 0 if s_b == 0
+ * Decoded value: q_i * s_b / S_enc.
+ *   packed  uint8 [rows, cols / 2]   two codes per byte, element 2i in the low nibble (8-byte aligned)
+ *   scales  uint8 [rows, cols / 16]  E4M3 codes
+ *   s_enc   fp32 [1], device, out
+ * cols % 16 == 0; x 16-byte aligned; ws: at least DMOE_WS_STATUS_BYTES + 4
+ * bytes (the tensor maximum is reduced there).
+ */
+dmoe_status dmoe_quantize_nvfp4(const void* x, int rows, int cols, uint8_t* packed, uint8_t* scales, float* s_enc,
+                                void* ws, size_t ws_bytes, dmoe_stream_t stream);
+
+/*
  * Chunk-wise tensor fingerprint ("NVIDIA fait passer ...", section "Méthodologie
  * de débogage du non-déterminisme": fingerprints computed on the GPU, with
  * shape, dtype and element count recorded, chunk-wise for order-sensitive

@@ -396,7 +396,7 @@ def mxfp8_quantize(x_bits):
     return vals.reshape(rows, cols), scales
 
 
-def nvfp4_quantize(x_bits):
+def nvfp4_quantize(x_bits, amax=None):
     """NVFP4 with two-level scaling, every step in binary32 in this order:
       amax_t   = max |x| over the tensor (finite inputs)
       S_enc    = 2688 / amax_t  (2688 = 448 * 6; 1 when amax_t == 0)
@@ -405,12 +405,16 @@ def nvfp4_quantize(x_bits):
         s_b     = E4M3( (amax_b / 6) * S_enc )      round to nearest even, saturating
         q_i     = E2M1( (x_i * S_enc) / value(s_b) )  (q_i = 0 when s_b encodes 0)
     Two E2M1 codes per byte, element 2i in the low nibble.
-    x_bits: bf16 bit patterns [rows, cols], cols % 16 == 0.
+    x_bits: bf16 bit patterns [rows, cols], cols % 16 == 0.  amax: the tensor
+    maximum when x_bits holds only some rows of the tensor.
     Returns (packed uint8 [rows, cols/2], scales uint8 [rows, cols/16], S_enc float32)."""
     x32 = bf16_to_f64(x_bits).astype(np.float32)
     rows, cols = x32.shape
     assert cols % NV_BLOCK == 0
-    amax_t = np.float32(np.abs(x32).max()) if x32.size else np.float32(0)
+    if amax is not None:
+        amax_t = np.float32(amax)
+    else:
+        amax_t = np.float32(np.abs(x32).max()) if x32.size else np.float32(0)
     s_enc = np.float32(1.0) if amax_t == 0 else np.float32(np.float32(2688.0) / amax_t)
     blk = x32.reshape(rows, cols // NV_BLOCK, NV_BLOCK)
     amax_b = np.abs(blk).max(axis=2)

@@ -30,7 +30,9 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for want in ["moe_grouped_gemm_fwd", "moe_grouped_gemm_dprob", "moe_grouped_gemm_dprob_atomic",
                  "moe_dprob_epilogue", "moe_dprob_combine", "dmoe_permute_indices", "dmoe_fingerprint",
-                 "dmoe_read_status", "dmoe_workspace_bytes", "moe_dispatch_gather", "moe_token_combine"]:
+                 "dmoe_read_status", "dmoe_workspace_bytes", "moe_dispatch_gather", "moe_token_combine",
+                 "moe_grouped_gemm_wgrad", "moe_grouped_gemm_dprob_serial", "dmoe_quantize_mxfp8",
+                 "dmoe_quantize_nvfp4"]:
         assert want in names
 
 
@@ -96,6 +98,18 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert c(16, 16, 16, 4, 0, 16, 16, None, 0, None) == 1    # topk = 0
     assert c(16, 16, 16, 4, 2, 16, 24, None, 0, None) == 1    # misaligned y
     assert c(None, None, None, 0, 2, 16, None, None, 0, None) == 0
+    q = lib.dmoe_quantize_mxfp8
+    q.argtypes = [P, I, I, P, P, P]
+    q.restype = I
+    assert q(16, 4, 48, 16, 16, None) == 2        # cols not a multiple of 32
+    assert q(8, 4, 64, 16, 16, None) == 1         # misaligned input
+    assert q(None, 0, 64, None, None, None) == 0  # empty: nothing to launch
+    v = lib.dmoe_quantize_nvfp4
+    v.argtypes = [P, I, I, P, P, P, P, SZ, P]
+    v.restype = I
+    assert v(16, 4, 24, 16, 16, 16, 16, 4096, None) == 2     # cols not a multiple of 16
+    assert v(16, 4, 32, 16, 16, None, 16, 4096, None) == 1   # no tensor-scale output
+    assert v(16, 4, 32, 16, 16, 16, 16, 200, None) == 6      # workspace below status + scratch
     fp = lib.dmoe_fingerprint
     fp.argtypes = [P, SZ, I, I, ctypes.POINTER(ctypes.c_int64), SZ, I, P, ctypes.POINTER(ctypes.c_uint64), P]
     fp.restype = I
