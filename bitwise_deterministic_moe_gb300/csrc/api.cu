@@ -70,6 +70,8 @@ dmoe_status cuda_status(cudaError_t e) {
 // counters (two ints, left at zero by every launch) at byte 64.
 int* status_ptr(void* ws) { return static_cast<int*>(ws); }
 int* sched_ptr(void* ws) { return reinterpret_cast<int*>(static_cast<char*>(ws) + 64); }
+// the routing block scan's finished-block counter at byte 128
+int* route_counter_ptr(void* ws) { return reinterpret_cast<int*>(static_cast<char*>(ws) + 128); }
 
 dmoe_status check_gemm_shape(const void* X, const void* W, const int32_t* off, int R, int E, int K, int N,
                              const void* out, void* ws, size_t ws_bytes) {
@@ -142,7 +144,7 @@ dmoe_status dmoe_permute_indices(const int32_t* topk_ids, int T, int topk, int E
   if (R > 0 && (!topk_ids || !row_src)) return DMOE_ERR_INVALID_ARG;
   if (!ws || ws_bytes < dmoe_workspace_bytes(T, topk, E)) return DMOE_ERR_WORKSPACE;
   void* scratch = static_cast<char*>(ws) + DMOE_WS_STATUS_BYTES;
-  return cuda_status(launch_permute(topk_ids, R, E, expert_offsets, row_src, row_of, scratch, status_ptr(ws),
+  return cuda_status(launch_permute(topk_ids, R, E, expert_offsets, row_src, row_of, scratch, status_ptr(ws), route_counter_ptr(ws),
                                     reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -57,8 +57,10 @@ size_t serial_flag_bytes(long long R, int E);
 
 // routing
 size_t routing_scratch_bytes(long long R, int E);
+// done_counter: one int of the workspace, zero between calls (the last block of
+// the block scan resets it)
 cudaError_t launch_permute(const int32_t* topk_ids, long long R, int E, int32_t* offsets, int32_t* row_src,
-                           int32_t* row_of, void* scratch, int* status, cudaStream_t stream);
+                           int32_t* row_of, void* scratch, int* status, int* done_counter, cudaStream_t stream);
 
 // dispatch gather and token combine (status may be null: errors not recorded)
 cudaError_t launch_dispatch_gather(const void* hidden, const int32_t* row_src, int R, int topk, int H,

@@ -64,3 +64,21 @@ def test_out_of_range_id_sets_routing_status():
     ids[17, 1] = -2
     _, _, st = run(ids, 8)
     assert st == 3
+
+
+def test_repeated_calls_share_one_workspace():
+    """The grid barrier words live in the workspace: calls of different sizes
+    (different grids) back to back on one workspace stay consistent."""
+    E = 64
+    ws = api.workspace(20000, 6, E)
+    rng = np.random.default_rng(11)
+    for it in range(24):
+        T = int(rng.integers(1, 20000))
+        ids_np = rng.integers(0, E, (T, 6)).astype(np.int32)
+        ids = torch.from_numpy(ids_np).cuda()
+        off, src, row_of = api.permute_indices(ids, E, ws, with_row_of=True)
+        roff, rsrc = oracle.routing(ids_np, E)
+        np.testing.assert_array_equal(off.cpu().numpy(), roff)
+        np.testing.assert_array_equal(src.cpu().numpy(), rsrc)
+        np.testing.assert_array_equal(row_of.cpu().numpy(), oracle.inverse_rows(rsrc))
+    assert api.read_status(ws) == 0
