@@ -355,6 +355,12 @@ __device__ __forceinline__ void st_cluster_s32(uint32_t cluster_addr, int v) {
 }
 
 // All threads of both CTAs of the pair (release/acquire at cluster scope).
+__device__ __forceinline__ unsigned long long ld_shared_cluster_u64(uint32_t cluster_addr) {
+  unsigned long long v;
+  asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(cluster_addr) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }

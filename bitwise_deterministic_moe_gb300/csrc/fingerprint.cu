@@ -15,6 +15,9 @@
 // Xor mode: xor of the chunk's elements widened to 64 bits, the reduction
 // torch.hash_tensor uses, also order-independent.
 //
+// One launch: each chunk is hashed by a cluster of eight CTAs, one part of
+// the chunk each; the parts' sums meet in distributed shared memory and the
+// cluster's first CTA finalizes the chunk -- no atomics, no zero-fill.
 // The pass is HBM-bound: 16-byte loads, about a dozen integer ops per word.
 #include <algorithm>
 
@@ -26,8 +29,9 @@
 namespace dmoe {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr size_t kPartBytes = 16 * 1024;   // bytes of one chunk handled by one CTA
+constexpr int kThreads = 1024;
+constexpr int kUnroll = 8;                 // 16-byte loads in flight per thread
+constexpr uint32_t kCluster = 8;           // CTAs (parts) per chunk, one cluster
 
 __device__ __forceinline__ uint32_t fmix32(uint32_t h) {
   h ^= h >> 16;
@@ -77,35 +81,47 @@ __device__ __forceinline__ uint64_t block_xor_u64(uint64_t v) {
   return t;
 }
 
-// 1-D grid, block = chunk * parts + part.  VEC: data is 16-byte aligned.
+// Grid: kCluster CTAs per chunk (a cluster), CTA r of chunk c hashes bytes
+// [c*chunk + r*part, ...) of the chunk.  VEC: data is 16-byte aligned.
 template <bool VEC>
 __global__ void __launch_bounds__(kThreads)
-fp_positional_kernel(const uint8_t* __restrict__ data, size_t nbytes, size_t chunk_bytes, unsigned parts,
-                     unsigned long long* __restrict__ acc) {
+fp_positional_kernel(const uint8_t* __restrict__ data, size_t nbytes, size_t chunk_bytes, size_t part_bytes,
+                     unsigned long long* __restrict__ out) {
+  __shared__ unsigned long long part_sum;
   pdl_begin();
-  const size_t c = blockIdx.x / parts;
-  const size_t b0 = c * chunk_bytes + size_t(blockIdx.x % parts) * kPartBytes;
+  const size_t c = blockIdx.x / kCluster;
+  const uint32_t rank = cluster_ctarank();
   const size_t chunk_end = min(nbytes, (c + 1) * chunk_bytes);
-  if (b0 >= chunk_end) return;
-  const size_t b1 = min(chunk_end, b0 + kPartBytes);
+  const size_t b0 = min(chunk_end, c * chunk_bytes + size_t(rank) * part_bytes);
+  const size_t b1 = min(chunk_end, b0 + part_bytes);
   uint64_t sum = 0;
-  // 16-byte groups fully inside [b0, b1)
+  // 16-byte groups fully inside [b0, b1), kUnroll of them in flight per thread
   const size_t nfull = (b1 - b0) / 16;
-  for (size_t v = threadIdx.x; v < nfull; v += kThreads) {
-    const size_t off = b0 + v * 16;
-    uint32_t w[4];
-    if (VEC) {
-      const uint4 q = ldg_nc_v4(data + off);
-      w[0] = q.x; w[1] = q.y; w[2] = q.z; w[3] = q.w;
-    } else {
+  for (size_t v0 = threadIdx.x; v0 < nfull; v0 += size_t(kThreads) * kUnroll) {
+    uint32_t w[kUnroll][4];
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
-        w[k] = uint32_t(data[off + 4 * k]) | (uint32_t(data[off + 4 * k + 1]) << 8) |
-               (uint32_t(data[off + 4 * k + 2]) << 16) | (uint32_t(data[off + 4 * k + 3]) << 24);
+    for (int u = 0; u < kUnroll; ++u) {
+      const size_t v = v0 + size_t(u) * kThreads;
+      if (v >= nfull) continue;
+      const size_t off = b0 + v * 16;
+      if (VEC) {
+        const uint4 q = ldg_nc_v4(data + off);
+        w[u][0] = q.x; w[u][1] = q.y; w[u][2] = q.z; w[u][3] = q.w;
+      } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          w[u][k] = uint32_t(data[off + 4 * k]) | (uint32_t(data[off + 4 * k + 1]) << 8) |
+                    (uint32_t(data[off + 4 * k + 2]) << 16) | (uint32_t(data[off + 4 * k + 3]) << 24);
+      }
     }
-    const uint64_t i0 = off / 4;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) sum += word_term(w[k], i0 + k);
+    for (int u = 0; u < kUnroll; ++u) {
+      const size_t v = v0 + size_t(u) * kThreads;
+      if (v >= nfull) continue;
+      const uint64_t i0 = (b0 + v * 16) / 4;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) sum += word_term(w[u][k], i0 + k);
+    }
   }
   // ragged tail (only at the very end of the buffer): words with 4i < b1
   if (threadIdx.x == 0) {
@@ -117,16 +133,15 @@ fp_positional_kernel(const uint8_t* __restrict__ data, size_t nbytes, size_t chu
     }
   }
   const uint64_t t = block_sum_u64(sum);
-  if (threadIdx.x == 0 && t != 0) atomicAdd(acc + c, (unsigned long long)t);
-}
-
-__global__ void fp_finalize_kernel(unsigned long long* __restrict__ acc, size_t nchunks, size_t nbytes,
-                                   size_t chunk_bytes) {
-  pdl_begin();
-  const size_t c = size_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (c >= nchunks) return;
-  const size_t len = min(chunk_bytes, nbytes - c * chunk_bytes);
-  acc[c] = sm64(acc[c] ^ (uint64_t(c) << 32) ^ uint64_t(len));
+  if (threadIdx.x == 0) part_sum = t;
+  cluster_sync_all();
+  if (rank == 0 && threadIdx.x == 0) {
+    uint64_t acc = 0;
+    for (uint32_t r = 0; r < kCluster; ++r) acc += ld_shared_cluster_u64(mapa_shared(smem_u32(&part_sum), r));
+    const size_t len = chunk_end - c * chunk_bytes;
+    out[c] = sm64(acc ^ (uint64_t(c) << 32) ^ uint64_t(len));
+  }
+  cluster_sync_all();   // no CTA leaves while the first one still reads its sum
 }
 
 // xor_kind: 0 unsigned, 1 signed, 2 float16, 3 bfloat16, 4 float32, 5 float64
@@ -153,19 +168,46 @@ __device__ __forceinline__ uint64_t widen(const uint8_t* p, int kind) {
 
 template <int ES>
 __global__ void __launch_bounds__(kThreads)
-fp_xor_kernel(const uint8_t* __restrict__ data, size_t nbytes, size_t chunk_bytes, unsigned parts, int kind,
-              unsigned long long* __restrict__ acc) {
+fp_xor_kernel(const uint8_t* __restrict__ data, size_t nbytes, size_t chunk_bytes, size_t part_bytes, int kind,
+              unsigned long long* __restrict__ out) {
+  __shared__ unsigned long long part_x;
   pdl_begin();
-  const size_t c = blockIdx.x / parts;
-  const size_t b0 = c * chunk_bytes + size_t(blockIdx.x % parts) * kPartBytes;
+  const size_t c = blockIdx.x / kCluster;
+  const uint32_t rank = cluster_ctarank();
   const size_t chunk_end = min(nbytes, (c + 1) * chunk_bytes);
-  if (b0 >= chunk_end) return;
-  const size_t b1 = min(chunk_end, b0 + kPartBytes);
+  const size_t b0 = min(chunk_end, c * chunk_bytes + size_t(rank) * part_bytes);
+  const size_t b1 = min(chunk_end, b0 + part_bytes);
   uint64_t x = 0;
   for (size_t off = b0 + size_t(threadIdx.x) * ES; off < b1; off += size_t(kThreads) * ES)
     x ^= widen<ES>(data + off, kind);
   const uint64_t t = block_xor_u64(x);
-  if (threadIdx.x == 0 && t != 0) atomicXor(acc + c, (unsigned long long)t);
+  if (threadIdx.x == 0) part_x = t;
+  cluster_sync_all();
+  if (rank == 0 && threadIdx.x == 0) {
+    uint64_t acc = 0;
+    for (uint32_t r = 0; r < kCluster; ++r) acc ^= ld_shared_cluster_u64(mapa_shared(smem_u32(&part_x), r));
+    out[c] = acc;
+  }
+  cluster_sync_all();
+}
+
+template <typename K, typename... Args>
+cudaError_t launch_clustered(K kernel, unsigned grid, cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 }  // namespace
@@ -174,31 +216,24 @@ cudaError_t launch_fingerprint(const void* data, size_t nbytes, int elem_size, i
                                int mode, uint64_t* chunk_hash, cudaStream_t stream) {
   const size_t nchunks = (nbytes + chunk_bytes - 1) / chunk_bytes;
   if (nchunks == 0) return cudaSuccess;
-  const size_t parts = (std::min(chunk_bytes, nbytes) + kPartBytes - 1) / kPartBytes;
-  if (nchunks * parts > 0x7FFFFFFFull) return cudaErrorInvalidValue;
-  cudaError_t e = cudaMemsetAsync(chunk_hash, 0, nchunks * sizeof(uint64_t), stream);
-  if (e != cudaSuccess) return e;
-  auto* acc = reinterpret_cast<unsigned long long*>(chunk_hash);
+  if (nchunks * kCluster > 0x7FFFFFFFull) return cudaErrorInvalidValue;
+  // parts are 16-byte multiples so that part starts keep the chunk's alignment
+  const size_t part = ((chunk_bytes + kCluster - 1) / kCluster + 15) / 16 * 16;
+  auto* out = reinterpret_cast<unsigned long long*>(chunk_hash);
   const uint8_t* d = static_cast<const uint8_t*>(data);
-  const unsigned grid = unsigned(nchunks * parts);
-  const unsigned np = unsigned(parts);
+  const unsigned grid = unsigned(nchunks * kCluster);
   if (mode == 0) {
     if ((reinterpret_cast<uintptr_t>(d) & 15) == 0)
-      e = launch_chained(fp_positional_kernel<true>, dim3(grid), dim3(kThreads), 0, stream, d, nbytes, chunk_bytes, np, acc);
-    else
-      e = launch_chained(fp_positional_kernel<false>, dim3(grid), dim3(kThreads), 0, stream, d, nbytes, chunk_bytes, np, acc);
-    if (e != cudaSuccess) return e;
-    return launch_chained(fp_finalize_kernel, dim3(unsigned((nchunks + 255) / 256)), dim3(256), 0, stream, acc, nchunks,
-                          nbytes, chunk_bytes);
+      return launch_clustered(fp_positional_kernel<true>, grid, stream, d, nbytes, chunk_bytes, part, out);
+    return launch_clustered(fp_positional_kernel<false>, grid, stream, d, nbytes, chunk_bytes, part, out);
   }
   switch (elem_size) {
-    case 1: return launch_chained(fp_xor_kernel<1>, dim3(grid), dim3(kThreads), 0, stream, d, nbytes, chunk_bytes, np, xor_kind, acc);
-    case 2: return launch_chained(fp_xor_kernel<2>, dim3(grid), dim3(kThreads), 0, stream, d, nbytes, chunk_bytes, np, xor_kind, acc);
-    case 4: return launch_chained(fp_xor_kernel<4>, dim3(grid), dim3(kThreads), 0, stream, d, nbytes, chunk_bytes, np, xor_kind, acc);
-    case 8: return launch_chained(fp_xor_kernel<8>, dim3(grid), dim3(kThreads), 0, stream, d, nbytes, chunk_bytes, np, xor_kind, acc);
+    case 1: return launch_clustered(fp_xor_kernel<1>, grid, stream, d, nbytes, chunk_bytes, part, xor_kind, out);
+    case 2: return launch_clustered(fp_xor_kernel<2>, grid, stream, d, nbytes, chunk_bytes, part, xor_kind, out);
+    case 4: return launch_clustered(fp_xor_kernel<4>, grid, stream, d, nbytes, chunk_bytes, part, xor_kind, out);
+    case 8: return launch_clustered(fp_xor_kernel<8>, grid, stream, d, nbytes, chunk_bytes, part, xor_kind, out);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace dmoe
