@@ -332,7 +332,9 @@ def run_ours(args):
     fp_src = torch.empty(api.fingerprint_num_chunks(R * 4), dtype=torch.int64, device=dev)
     fp_dp = torch.empty(api.fingerprint_num_chunks(R * 4), dtype=torch.int64, device=dev)
     stream = torch.cuda.current_stream(dev)
-    launches_per_step = 4 + 2 + 2 + 2   # routing 4, fingerprint 2, GEMM + combine 2, fingerprint 2
+    # routing 3 (histogram, block scan with offsets, scatter), fingerprint 1,
+    # GEMM + slot combine 2, fingerprint 1
+    launches_per_step = 3 + 1 + 2 + 1
 
     def step(ev=None):
         api.permute_indices(ids, cfg.E, ws, off, src, row_of=row_of)
