@@ -18,7 +18,8 @@
 // s_b = E4M3((amax_b / 6) * S_enc); q_i = E2M1((x_i * S_enc) / value(s_b)),
 // 0 when s_b is 0; two E2M1 codes per byte, element 2i in the low nibble.
 //
-// Both passes are HBM-bound: 16-byte loads, one thread per block.
+// Both passes are HBM-bound: 16-byte loads, one thread per block (the NVFP4
+// encode pass also carries sixteen correctly rounded divisions per block).
 #include "common.cuh"
 #include "internal.h"
 
@@ -124,11 +125,21 @@ __global__ void __launch_bounds__(kThreads)
 amax_kernel(const uint4* __restrict__ x, long long nvec, unsigned int* __restrict__ amax_bits) {
   pdl_begin();
   float m = 0.f;
-  for (long long i = blockIdx.x * (long long)kThreads + threadIdx.x; i < nvec; i += (long long)gridDim.x * kThreads) {
-    float t[8];
-    unpack8(ldg_nc_v4(x + i), t);
+  const long long stride = (long long)gridDim.x * kThreads;
+  for (long long i0 = blockIdx.x * (long long)kThreads + threadIdx.x; i0 < nvec; i0 += stride * 8) {
+    uint4 q[8];   // eight 16-byte loads in flight per thread
 #pragma unroll
-    for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(t[j]));
+    for (int u = 0; u < 8; ++u) {
+      const long long i = i0 + u * stride;
+      q[u] = i < nvec ? ldg_nc_v4(x + i) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      float t[8];
+      unpack8(q[u], t);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(t[j]));
+    }
   }
 #pragma unroll
   for (int d = 16; d > 0; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
@@ -142,15 +153,27 @@ nvfp4_kernel(const uint4* __restrict__ x, long long nblocks, const unsigned int*
   const float amax_t = __uint_as_float(*amax_bits);
   const float s_enc = amax_t > 0.f ? __fdiv_rn(2688.0f, amax_t) : 1.0f;
   if (blockIdx.x == 0 && threadIdx.x == 0) *s_enc_out = s_enc;
-  for (long long b = blockIdx.x * (long long)kThreads + threadIdx.x; b < nblocks;
-       b += (long long)gridDim.x * kThreads) {
+  const long long stride = (long long)gridDim.x * kThreads;
+  for (long long b0 = blockIdx.x * (long long)kThreads + threadIdx.x; b0 < nblocks; b0 += stride * 2) {
+    // two blocks per thread per round: four 16-byte loads in flight
+    uint4 in[2][2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const long long b = b0 + u * stride;
+      in[u][0] = b < nblocks ? ldg_nc_v4(x + b * 2) : make_uint4(0u, 0u, 0u, 0u);
+      in[u][1] = b < nblocks ? ldg_nc_v4(x + b * 2 + 1) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+    const long long b = b0 + u * stride;
+    if (b >= nblocks) break;
     float f[16];
     {
       float t[8];
-      unpack8(ldg_nc_v4(x + b * 2), t);
+      unpack8(in[u][0], t);
 #pragma unroll
       for (int j = 0; j < 8; ++j) f[j] = t[j];
-      unpack8(ldg_nc_v4(x + b * 2 + 1), t);
+      unpack8(in[u][1], t);
 #pragma unroll
       for (int j = 0; j < 8; ++j) f[8 + j] = t[j];
     }
@@ -171,6 +194,7 @@ nvfp4_kernel(const uint4* __restrict__ x, long long nblocks, const unsigned int*
     }
     packed[b] = make_uint2(pack_e2m1x8(h0), pack_e2m1x8(h1));
     scales[b] = sb;
+    }
   }
 }
 

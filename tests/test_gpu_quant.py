@@ -115,3 +115,28 @@ def test_latent_operands_sampled_rows(which):
     assert host(s_enc).view(np.uint32)[0] == np.float32(re).view(np.uint32)
     assert np.array_equal(host(packed.index_select(0, idx)), rp)
     assert np.array_equal(host(nscales.index_select(0, idx)), rns)
+
+
+def test_nvfp4_rounding_ties_and_boundaries():
+    """Blocks whose scaled values land exactly on E2M1 rounding boundaries
+    (0.25, 0.75, 1.25, ... : ties to even) and just beside them: the encoder's
+    quotient shortcut must hand these to the exact division and match the
+    oracle byte for byte."""
+    rows, cols = 64, 512
+    rng = np.random.default_rng(21)
+    v = np.zeros((rows, cols), dtype=np.float32)
+    for r in range(rows):
+        for b in range(cols // 16):
+            j = int(rng.integers(-20, 20))
+            k = rng.integers(0, 25, 16).astype(np.float32)      # multiples of 1/4 up to 6
+            k[0] = 24.0                                         # block max = 6 * 2^j
+            sign = np.where(rng.random(16) < 0.5, -1.0, 1.0).astype(np.float32)
+            nudge = np.float32(1.0) + rng.choice([0.0, 2.0 ** -7, -(2.0 ** -8)], 16).astype(np.float32)
+            nudge[0] = 1.0
+            v[r, b * 16:(b + 1) * 16] = sign * (k / 4) * np.float32(2.0 ** j) * nudge
+    x = synth.f32_to_bf16_bits(v)
+    ws = api.workspace(1, 1, 1)
+    packed, scales, s_enc = api.quantize_nvfp4(bf16_dev(x), ws)
+    rp, rs, re = oracle.nvfp4_quantize(x)
+    assert np.array_equal(host(scales), rs)
+    assert np.array_equal(host(packed), rp)
