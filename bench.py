@@ -220,6 +220,28 @@ def run_reference(args):
     return 0
 
 
+def _mix64(z: int) -> int:
+    """splitmix64's output function (folds chunk hashes into one digest)."""
+    m = (1 << 64) - 1
+    z &= m
+    z ^= z >> 30
+    z = (z * 0xBF58476D1CE4E5B9) & m
+    z ^= z >> 27
+    z = (z * 0x94D049BB133111EB) & m
+    z ^= z >> 31
+    return z
+
+
+def output_digest(api, t):
+    """One 64-bit digest of a device tensor: its fingerprint header folded with
+    every 1 MiB chunk hash, in chunk order (hex)."""
+    chunks, header = api.fingerprint_host(t)
+    h = header
+    for c in chunks:
+        h = _mix64(h ^ c)
+    return "%016x" % h
+
+
 def dispatch_combine(api, cfg, inp, src, row_of, expert_out, timed, dev, iters):
     """HBM roofline of the dispatch gather (hidden [T,N] -> x_perm [R,N]) and
     the token combine (expert_out [R,N] -> y [T,N]) on the step's routing and
@@ -469,6 +491,12 @@ def run_ours(args):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": e_ms / args.e2e_steps}
 
+    # digests of the step's outputs (chunk fingerprints folded with the header):
+    # identical inputs give identical digests on every run
+    fingerprints = {name: output_digest(api, t) for name, t in
+                    (("row_src", src), ("expert_offsets", off), ("expert_out", out), ("slots", slots),
+                     ("dprob", dprob))}
+
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -511,6 +539,7 @@ def run_ours(args):
         "quantize": qz,
         "e2e": e2e,
         "clocks": clocks,
+        "fingerprints": fingerprints,
     }
     if base is not None:
         line["cpu_baseline"] = base
