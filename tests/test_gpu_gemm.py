@@ -25,6 +25,14 @@ SHAPES = [
     synth.custom_config("wide", T=300, E=5, topk=2, K=72, N=1024, index=302),      # K < one stage
     synth.custom_config("manyexp", T=700, E=1024, topk=8, K=128, N=256, index=303),  # many small experts
     synth.custom_config("zipf", T=1024, E=64, topk=6, K=256, N=512, routing="zipf", index=304),
+    synth.custom_config("n128", T=400, E=6, topk=2, K=192, N=128, index=306),       # one slot, half N-tile only
+]
+
+# large dimensions (index arithmetic past 2^31 bytes of W, deep K, wide N), sampled rows
+LARGE = [
+    synth.custom_config("wideN", T=96, E=4, topk=2, K=128, N=8192, index=307),
+    synth.custom_config("deepK", T=160, E=8, topk=3, K=8192, N=256, index=308),
+    synth.custom_config("bigW", T=256, E=1024, topk=2, K=4096, N=512, index=309),  # W = 4 GiB
 ]
 
 
@@ -181,3 +189,13 @@ def test_serialized_writers_full_size(name):
                                                    prob.ws)
         assert api.read_status(prob.ws) == 0
         assert torch.equal(dprob.view(torch.int32), dprob_s.view(torch.int32))
+
+
+@pytest.mark.parametrize("flags", KERNELS, ids=KERNEL_IDS)
+@pytest.mark.parametrize("cfg", LARGE, ids=[c.name for c in LARGE])
+def test_large_dimensions(cfg, flags):
+    prob = Problem(cfg)
+    out, dprob, slots = prob.run_dprob(flags=flags)
+    assert api.read_status(prob.ws) == 0
+    off = prob.off.cpu().numpy()
+    gpu_util.check_rows_against_oracle(prob, out, slots, dprob, gpu_util.sample_rows(off, 48, seed=cfg.seed))

@@ -80,6 +80,8 @@ SHAPES = [
     synth.custom_config("ragged", T=600, E=12, topk=3, K=320, N=384, index=301),   # column tile 2 of 2 partial
     synth.custom_config("wide", T=300, E=5, topk=2, K=72, N=1024, index=302),      # K < one box pair
     synth.custom_config("zipf", T=1024, E=64, topk=6, K=256, N=512, routing="zipf", index=304),
+    synth.custom_config("n128", T=400, E=6, topk=2, K=192, N=128, index=306),
+    synth.custom_config("deepN", T=64, E=3, topk=2, K=64, N=8192, index=310),
 ]
 
 
