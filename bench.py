@@ -289,6 +289,25 @@ def wgrad_measure(api, cfg, X, dY, off, ws, timed, dev, iters):
             "tensor_frac": flops / (ms * 1e-3) / 1e12 / pk["bf16_tflops"]}
 
 
+def passes_measure(api, cfg, out, slots, src, timed, iters):
+    """The HBM passes of the path on buffers of the workload: the chunk
+    fingerprint of expert_out (R*N*2 bytes, larger than L2) and the
+    fixed-order slot combine (slots S*R*4 read, row_src and dprob R*4 each)."""
+    import torch
+    pk, _ = peaks()
+    fp = torch.empty(api.fingerprint_num_chunks(out.numel() * 2), dtype=torch.int64, device=out.device)
+    dp = torch.empty(cfg.T, cfg.topk, dtype=torch.float32, device=out.device)
+    res = {}
+    for name, fn, b in (("fingerprint_expert_out", lambda: api.fingerprint(out, out=fp), out.numel() * 2),
+                        ("slot_combine", lambda: api.dprob_combine(slots, src, cfg.topk, dprob=dp),
+                         cfg.S * cfg.R * 4 + 2 * cfg.R * 4)):
+        ms = timed(fn, iters)
+        gbs = b / (ms * 1e-3) / 1e9
+        res[name] = {"ms": ms, "algorithmic_bytes": b, "achieved_gbs": gbs, "peak_gbs": pk["hbm_gbs"],
+                     "frac": gbs / pk["hbm_gbs"]}
+    return res
+
+
 def quant_measure(api, X, ws, timed, iters):
     """MXFP8 and NVFP4 encodings of the step's X_perm [R, K] bf16.  Algorithmic
     bytes: MXFP8 reads X once and writes R*K codes + R*K/32 scales; NVFP4 reads X
@@ -458,6 +477,7 @@ def run_ours(args):
                                                               args.tax_iters)
     wg = None if args.skip_wgrad else wgrad_measure(api, cfg, X, out, off, ws, timed, dev, args.tax_iters)
     qz = None if args.skip_quant else quant_measure(api, X, ws, timed, args.tax_iters)
+    hp = passes_measure(api, cfg, out, slots, src, timed, args.tax_iters)
 
     # ---------------- end to end through the public API, host buffers
     e2e = None
@@ -542,6 +562,7 @@ def run_ours(args):
         "dispatch_combine": around,
         "wgrad": wg,
         "quantize": qz,
+        "hbm_passes": hp,
         "e2e": e2e,
         "clocks": clocks,
         "fingerprints": fingerprints,

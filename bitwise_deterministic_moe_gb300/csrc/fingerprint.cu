@@ -17,7 +17,8 @@
 //
 // One launch: each chunk is hashed by a cluster of eight CTAs, one part of
 // the chunk each; the parts' sums meet in distributed shared memory and the
-// cluster's first CTA finalizes the chunk -- no atomics, no zero-fill.
+// cluster's first CTA finalizes the chunk -- no atomics, no zero-fill.  The
+// clusters are persistent (as many as fit) and loop over the chunks.
 // The pass is HBM-bound: 16-byte loads, about a dozen integer ops per word.
 #include <algorithm>
 
@@ -29,8 +30,12 @@
 namespace dmoe {
 namespace {
 
-constexpr int kThreads = 1024;
 constexpr int kUnroll = 8;                 // 16-byte loads in flight per thread
+// CTA size: 1024 threads cut the latency of one-chunk buffers; 128 threads
+// (more CTAs and clusters resident) stream large buffers faster.
+constexpr int kThreadsFew = 1024;
+constexpr int kThreadsMany = 128;
+constexpr size_t kFewChunks = 8;
 constexpr uint32_t kCluster = 8;           // CTAs (parts) per chunk, one cluster
 
 __device__ __forceinline__ uint32_t fmix32(uint32_t h) {
@@ -55,6 +60,7 @@ __device__ __forceinline__ uint64_t word_term(uint32_t w, uint64_t i) {
   return fmix32(w ^ (uint32_t(i) * 0x9E3779B9u));
 }
 
+template <int kThreads>
 __device__ __forceinline__ uint64_t block_sum_u64(uint64_t v) {
   __shared__ uint64_t ws[kThreads / 32];
 #pragma unroll
@@ -68,6 +74,7 @@ __device__ __forceinline__ uint64_t block_sum_u64(uint64_t v) {
   return t;
 }
 
+template <int kThreads>
 __device__ __forceinline__ uint64_t block_xor_u64(uint64_t v) {
   __shared__ uint64_t ws[kThreads / 32];
 #pragma unroll
@@ -81,16 +88,19 @@ __device__ __forceinline__ uint64_t block_xor_u64(uint64_t v) {
   return t;
 }
 
-// Grid: kCluster CTAs per chunk (a cluster), CTA r of chunk c hashes bytes
-// [c*chunk + r*part, ...) of the chunk.  VEC: data is 16-byte aligned.
-template <bool VEC>
+// Grid: persistent clusters of kCluster CTAs; cluster k hashes chunks k,
+// k + nclusters, ...; CTA r hashes bytes [c*chunk + r*part, ...) of chunk c.
+// VEC: data is 16-byte aligned.
+template <bool VEC, int kThreads>
 __global__ void __launch_bounds__(kThreads)
 fp_positional_kernel(const uint8_t* __restrict__ data, size_t nbytes, size_t chunk_bytes, size_t part_bytes,
-                     unsigned long long* __restrict__ out) {
-  __shared__ unsigned long long part_sum;
+                     unsigned long long* __restrict__ out, size_t nchunks) {
+  __shared__ unsigned long long part_sum[2];   // double-buffered by chunk parity: one cluster barrier per chunk
   pdl_begin();
-  const size_t c = blockIdx.x / kCluster;
   const uint32_t rank = cluster_ctarank();
+  const size_t nclusters = gridDim.x / kCluster;
+  int it = 0;
+  for (size_t c = blockIdx.x / kCluster; c < nchunks; c += nclusters, ++it) {
   const size_t chunk_end = min(nbytes, (c + 1) * chunk_bytes);
   const size_t b0 = min(chunk_end, c * chunk_bytes + size_t(rank) * part_bytes);
   const size_t b1 = min(chunk_end, b0 + part_bytes);
@@ -132,16 +142,18 @@ fp_positional_kernel(const uint8_t* __restrict__ data, size_t nbytes, size_t chu
       sum += word_term(w, off / 4);
     }
   }
-  const uint64_t t = block_sum_u64(sum);
-  if (threadIdx.x == 0) part_sum = t;
-  cluster_sync_all();
+  const uint64_t t = block_sum_u64<kThreads>(sum);
+  if (threadIdx.x == 0) part_sum[it & 1] = t;
+  cluster_sync_all();   // also keeps block_sum's scratch from being reused early
   if (rank == 0 && threadIdx.x == 0) {
     uint64_t acc = 0;
-    for (uint32_t r = 0; r < kCluster; ++r) acc += ld_shared_cluster_u64(mapa_shared(smem_u32(&part_sum), r));
+    for (uint32_t r = 0; r < kCluster; ++r)
+      acc += ld_shared_cluster_u64(mapa_shared(smem_u32(&part_sum[it & 1]), r));
     const size_t len = chunk_end - c * chunk_bytes;
     out[c] = sm64(acc ^ (uint64_t(c) << 32) ^ uint64_t(len));
   }
-  cluster_sync_all();   // no CTA leaves while the first one still reads its sum
+  }
+  cluster_sync_all();   // no CTA leaves while the first one still reads its sums
 }
 
 // xor_kind: 0 unsigned, 1 signed, 2 float16, 3 bfloat16, 4 float32, 5 float64
@@ -166,35 +178,40 @@ __device__ __forceinline__ uint64_t widen(const uint8_t* p, int kind) {
   }
 }
 
-template <int ES>
+template <int ES, int kThreads>
 __global__ void __launch_bounds__(kThreads)
 fp_xor_kernel(const uint8_t* __restrict__ data, size_t nbytes, size_t chunk_bytes, size_t part_bytes, int kind,
-              unsigned long long* __restrict__ out) {
-  __shared__ unsigned long long part_x;
+              unsigned long long* __restrict__ out, size_t nchunks) {
+  __shared__ unsigned long long part_x[2];
   pdl_begin();
-  const size_t c = blockIdx.x / kCluster;
   const uint32_t rank = cluster_ctarank();
+  const size_t nclusters = gridDim.x / kCluster;
+  int it = 0;
+  for (size_t c = blockIdx.x / kCluster; c < nchunks; c += nclusters, ++it) {
   const size_t chunk_end = min(nbytes, (c + 1) * chunk_bytes);
   const size_t b0 = min(chunk_end, c * chunk_bytes + size_t(rank) * part_bytes);
   const size_t b1 = min(chunk_end, b0 + part_bytes);
   uint64_t x = 0;
   for (size_t off = b0 + size_t(threadIdx.x) * ES; off < b1; off += size_t(kThreads) * ES)
     x ^= widen<ES>(data + off, kind);
-  const uint64_t t = block_xor_u64(x);
-  if (threadIdx.x == 0) part_x = t;
+  const uint64_t t = block_xor_u64<kThreads>(x);
+  if (threadIdx.x == 0) part_x[it & 1] = t;
   cluster_sync_all();
   if (rank == 0 && threadIdx.x == 0) {
     uint64_t acc = 0;
-    for (uint32_t r = 0; r < kCluster; ++r) acc ^= ld_shared_cluster_u64(mapa_shared(smem_u32(&part_x), r));
+    for (uint32_t r = 0; r < kCluster; ++r) acc ^= ld_shared_cluster_u64(mapa_shared(smem_u32(&part_x[it & 1]), r));
     out[c] = acc;
+  }
   }
   cluster_sync_all();
 }
 
-template <typename K, typename... Args>
-cudaError_t launch_clustered(K kernel, unsigned grid, cudaStream_t stream, Args... args) {
+// Clusters are persistent: as many as can be resident at once (capped by the
+// number of chunks), each looping over chunks.
+template <int kThreads, typename K, typename... Args>
+cudaError_t launch_clustered(K kernel, size_t nchunks, cudaStream_t stream, Args... args) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
+  cfg.gridDim = dim3(kCluster);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
@@ -207,7 +224,18 @@ cudaError_t launch_clustered(K kernel, unsigned grid, cudaStream_t stream, Args.
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kernel, args...);
+  static int max_clusters = 0;   // per kernel instantiation
+  if (max_clusters == 0) {
+    int n = 0;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
+    cfg.numAttrs = 2;
+    if (e != cudaSuccess) return e;
+    max_clusters = n > 0 ? n : 1;
+  }
+  const size_t clusters = nchunks < size_t(max_clusters) ? nchunks : size_t(max_clusters);
+  cfg.gridDim = dim3(unsigned(clusters * kCluster));
+  return cudaLaunchKernelEx(&cfg, kernel, args..., nchunks);
 }
 
 }  // namespace
@@ -221,17 +249,31 @@ cudaError_t launch_fingerprint(const void* data, size_t nbytes, int elem_size, i
   const size_t part = ((chunk_bytes + kCluster - 1) / kCluster + 15) / 16 * 16;
   auto* out = reinterpret_cast<unsigned long long*>(chunk_hash);
   const uint8_t* d = static_cast<const uint8_t*>(data);
-  const unsigned grid = unsigned(nchunks * kCluster);
+  const bool few = nchunks <= kFewChunks;
   if (mode == 0) {
-    if ((reinterpret_cast<uintptr_t>(d) & 15) == 0)
-      return launch_clustered(fp_positional_kernel<true>, grid, stream, d, nbytes, chunk_bytes, part, out);
-    return launch_clustered(fp_positional_kernel<false>, grid, stream, d, nbytes, chunk_bytes, part, out);
+    const bool vec = (reinterpret_cast<uintptr_t>(d) & 15) == 0;
+    if (few)
+      return vec ? launch_clustered<kThreadsFew>(fp_positional_kernel<true, kThreadsFew>, nchunks, stream, d, nbytes,
+                                                 chunk_bytes, part, out)
+                 : launch_clustered<kThreadsFew>(fp_positional_kernel<false, kThreadsFew>, nchunks, stream, d, nbytes,
+                                                 chunk_bytes, part, out);
+    return vec ? launch_clustered<kThreadsMany>(fp_positional_kernel<true, kThreadsMany>, nchunks, stream, d, nbytes,
+                                                chunk_bytes, part, out)
+               : launch_clustered<kThreadsMany>(fp_positional_kernel<false, kThreadsMany>, nchunks, stream, d, nbytes,
+                                                chunk_bytes, part, out);
   }
   switch (elem_size) {
-    case 1: return launch_clustered(fp_xor_kernel<1>, grid, stream, d, nbytes, chunk_bytes, part, xor_kind, out);
-    case 2: return launch_clustered(fp_xor_kernel<2>, grid, stream, d, nbytes, chunk_bytes, part, xor_kind, out);
-    case 4: return launch_clustered(fp_xor_kernel<4>, grid, stream, d, nbytes, chunk_bytes, part, xor_kind, out);
-    case 8: return launch_clustered(fp_xor_kernel<8>, grid, stream, d, nbytes, chunk_bytes, part, xor_kind, out);
+#define DMOE_FP_XOR(ES)                                                                                        \
+  case ES:                                                                                                     \
+    return few ? launch_clustered<kThreadsFew>(fp_xor_kernel<ES, kThreadsFew>, nchunks, stream, d, nbytes,     \
+                                               chunk_bytes, part, xor_kind, out)                               \
+               : launch_clustered<kThreadsMany>(fp_xor_kernel<ES, kThreadsMany>, nchunks, stream, d, nbytes,   \
+                                                chunk_bytes, part, xor_kind, out);
+    DMOE_FP_XOR(1)
+    DMOE_FP_XOR(2)
+    DMOE_FP_XOR(4)
+    DMOE_FP_XOR(8)
+#undef DMOE_FP_XOR
     default: return cudaErrorInvalidValue;
   }
 }
