@@ -26,6 +26,33 @@ int device_sm_count() {
   return cache[dev];
 }
 
+cudaError_t ensure_kernel_smem(const void* kernel, int bytes) {
+  static std::mutex mu;
+  static std::vector<std::pair<const void*, int>> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const auto& d : done)
+    if (d.first == kernel && d.second == dev) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.emplace_back(kernel, dev);
+  return e;
+}
+
+int cached_per_device(const void* key, int (*compute)()) {
+  static std::mutex mu;
+  static std::vector<std::pair<std::pair<const void*, int>, int>> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const auto& c : cache)
+    if (c.first.first == key && c.first.second == dev) return c.second;
+  const int v = compute();
+  if (v > 0) cache.push_back({{key, dev}, v});
+  return v;
+}
+
 namespace {
 
 uint64_t sm64_host(uint64_t z) {

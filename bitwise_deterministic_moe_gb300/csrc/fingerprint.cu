@@ -21,6 +21,7 @@
 // clusters are persistent (as many as fit) and loop over the chunks.
 // The pass is HBM-bound: 16-byte loads, about a dozen integer ops per word.
 #include <algorithm>
+#include <mutex>
 
 #include <cuda_fp16.h>
 
@@ -224,15 +225,25 @@ cudaError_t launch_clustered(K kernel, size_t nchunks, cudaStream_t stream, Args
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  static int max_clusters = 0;   // per kernel instantiation
-  if (max_clusters == 0) {
-    int n = 0;
-    cfg.numAttrs = 1;
-    const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
-    cfg.numAttrs = 2;
-    if (e != cudaSuccess) return e;
-    max_clusters = n > 0 ? n : 1;
+  // resident clusters of this kernel on this device (queried once per device)
+  static cudaLaunchConfig_t occ_cfg;
+  static cudaLaunchAttribute occ_attr;
+  static K occ_kernel;
+  static std::mutex occ_mu;
+  int max_clusters;
+  {
+    std::lock_guard<std::mutex> lock(occ_mu);
+    occ_cfg = cfg;
+    occ_attr = attr[0];
+    occ_cfg.attrs = &occ_attr;
+    occ_cfg.numAttrs = 1;
+    occ_kernel = kernel;
+    max_clusters = cached_per_device(reinterpret_cast<const void*>(kernel), []() {
+      int n = 0;
+      return cudaOccupancyMaxActiveClusters(&n, occ_kernel, &occ_cfg) == cudaSuccess ? n : 0;
+    });
   }
+  if (max_clusters <= 0) max_clusters = 1;
   const size_t clusters = nchunks < size_t(max_clusters) ? nchunks : size_t(max_clusters);
   cfg.gridDim = dim3(unsigned(clusters * kCluster));
   return cudaLaunchKernelEx(&cfg, kernel, args..., nchunks);

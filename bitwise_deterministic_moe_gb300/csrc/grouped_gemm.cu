@@ -534,13 +534,8 @@ namespace {
 template <int MODE>
 cudaError_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const KParams& kp, int grid,
                         cudaStream_t stream) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(kSmemBytes));
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  const cudaError_t e = ensure_kernel_smem(reinterpret_cast<const void*>(grouped_gemm_kernel<MODE>), int(kSmemBytes));
+  if (e != cudaSuccess) return e;
   return launch_chained(grouped_gemm_kernel<MODE>, dim3(grid), dim3(NUM_THREADS), kSmemBytes, stream, ta, tb, kp);
 }
 

@@ -515,13 +515,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
 template <int MODE>
 cudaError_t launch_pair_mode(const CUtensorMap& ta, const CUtensorMap& tb, const KParams& kp, int grid,
                              cudaStream_t stream) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_pair_kernel<MODE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  const cudaError_t e =
+      ensure_kernel_smem(reinterpret_cast<const void*>(grouped_gemm_pair_kernel<MODE>), int(kSmemBytes));
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(grid), 1, 1);
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);
@@ -539,33 +535,34 @@ cudaError_t launch_pair_mode(const CUtensorMap& ta, const CUtensorMap& tb, const
   return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<MODE>, ta, tb, kp);
 }
 
-// Largest even CTA count whose pairs can all be resident at once.
+// Largest even CTA count whose pairs can all be resident at once (per device).
+template <int MODE>
+int compute_resident_pair_ctas() {
+  if (ensure_kernel_smem(reinterpret_cast<const void*>(grouped_gemm_pair_kernel<MODE>), int(kSmemBytes)) !=
+      cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(device_sm_count() & ~1), 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, grouped_gemm_pair_kernel<MODE>, &cfg) != cudaSuccess || clusters < 1)
+    clusters = device_sm_count() / 2;
+  return 2 * clusters;
+}
+
 template <int MODE>
 int resident_pair_ctas() {
-  static int cached[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 2;
-  if (cached[dev] == 0) {
-    cudaFuncSetAttribute(grouped_gemm_pair_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         int(kSmemBytes));
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(unsigned(device_sm_count() & ~1), 1, 1);
-    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, grouped_gemm_pair_kernel<MODE>, &cfg) != cudaSuccess ||
-        clusters < 1)
-      clusters = device_sm_count() / 2;
-    cached[dev] = 2 * clusters;
-  }
-  return cached[dev];
+  const int n = cached_per_device(reinterpret_cast<const void*>(grouped_gemm_pair_kernel<MODE>),
+                                  compute_resident_pair_ctas<MODE>);
+  return n > 0 ? n : 2;
 }
 
 template <int MODE>

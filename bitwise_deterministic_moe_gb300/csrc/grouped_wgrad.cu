@@ -436,13 +436,8 @@ cudaError_t launch_grouped_wgrad(const WgradArgs& a, cudaStream_t stream) {
   kp.sched = a.sched;
   kp.wait_ns = kWaitLimitNs;
   if (!kp.sched) return cudaErrorInvalidValue;
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_wgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(kSmemBytes));
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  const cudaError_t e = ensure_kernel_smem(reinterpret_cast<const void*>(grouped_wgrad_kernel), int(kSmemBytes));
+  if (e != cudaSuccess) return e;
   const int grid = a.num_ctas > 0 ? a.num_ctas : device_sm_count();
   return launch_chained(grouped_wgrad_kernel, dim3(grid), dim3(NUM_THREADS), kSmemBytes, stream, tdy, tx, tdw, kp);
 }

@@ -81,4 +81,11 @@ cudaError_t launch_fingerprint(const void* data, size_t nbytes, int elem_size, i
 
 int device_sm_count();
 
+// One-time per-device setup of launchers, safe with several host threads and
+// several GPUs in one process: the dynamic shared-memory limit of a kernel
+// (set once per kernel and device), and a per-(key, device) cached integer
+// (computed by `compute` on first use; a value <= 0 is not cached).
+cudaError_t ensure_kernel_smem(const void* kernel, int bytes);
+int cached_per_device(const void* key, int (*compute)());
+
 }  // namespace dmoe

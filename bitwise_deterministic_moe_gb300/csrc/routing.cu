@@ -187,11 +187,9 @@ cudaError_t launch_permute(const int32_t* topk_ids, long long R, int E, int32_t*
                        stream, counts, E, nblk, totals, offsets, done_counter);
   if (e == cudaSuccess && nblk > 0) {
     const size_t smem = size_t(33) * E * sizeof(int);
-    static size_t smem_set = 0;
-    if (smem > 48 * 1024 && smem > smem_set) {
-      e = cudaFuncSetAttribute(scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(33 * DMOE_MAX_EXPERTS * sizeof(int)));
+    if (smem > 48 * 1024) {
+      e = ensure_kernel_smem(reinterpret_cast<const void*>(scatter_kernel), int(33 * DMOE_MAX_EXPERTS * sizeof(int)));
       if (e != cudaSuccess) return e;
-      smem_set = 33 * DMOE_MAX_EXPERTS * sizeof(int);
     }
     e = launch_chained(scatter_kernel, dim3(nblk), dim3(kEntriesPerBlock), smem, stream, topk_ids, R, E, nblk,
                        counts, offsets, row_src, row_of);
