@@ -18,8 +18,11 @@
 // s_b = E4M3((amax_b / 6) * S_enc); q_i = E2M1((x_i * S_enc) / value(s_b)),
 // 0 when s_b is 0; two E2M1 codes per byte, element 2i in the low nibble.
 //
-// Both passes are HBM-bound: 16-byte loads, one thread per block (the NVFP4
-// encode pass also carries sixteen correctly rounded divisions per block).
+// Both passes are HBM-bound: 16-byte loads, one thread per block.  The NVFP4
+// encode pass divides by the block scale through one correctly rounded
+// reciprocal per block and a two-fma correction per element (block_scale.cuh),
+// on the packed fp32x2 pipe, instead of sixteen divisions.
+#include "block_scale.cuh"
 #include "common.cuh"
 #include "internal.h"
 
@@ -146,6 +149,15 @@ amax_kernel(const uint4* __restrict__ x, long long nvec, unsigned int* __restric
   if ((threadIdx.x & 31) == 0 && m > 0.f) atomicMax(amax_bits, __float_as_uint(m));
 }
 
+// |x| maximum of eight packed bf16 pairs, as fp32 (max of non-negative values is exact in bf16)
+__device__ __forceinline__ float block_amax16(const uint4& p0, const uint4& p1) {
+  const uint32_t w[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) asm("max.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(w[i] & 0x7FFF7FFFu));
+  return fmaxf(bf16lo(m), bf16hi(m));
+}
+
 __global__ void __launch_bounds__(kThreads)
 nvfp4_kernel(const uint4* __restrict__ x, long long nblocks, const unsigned int* __restrict__ amax_bits,
              uint2* __restrict__ packed, uint8_t* __restrict__ scales, float* __restrict__ s_enc_out) {
@@ -153,6 +165,7 @@ nvfp4_kernel(const uint4* __restrict__ x, long long nblocks, const unsigned int*
   const float amax_t = __uint_as_float(*amax_bits);
   const float s_enc = amax_t > 0.f ? __fdiv_rn(2688.0f, amax_t) : 1.0f;
   if (blockIdx.x == 0 && threadIdx.x == 0) *s_enc_out = s_enc;
+  const float2 s_enc2 = make_float2(s_enc, s_enc);
   const long long stride = (long long)gridDim.x * kThreads;
   for (long long b0 = blockIdx.x * (long long)kThreads + threadIdx.x; b0 < nblocks; b0 += stride * 2) {
     // two blocks per thread per round: four 16-byte loads in flight
@@ -165,35 +178,31 @@ nvfp4_kernel(const uint4* __restrict__ x, long long nblocks, const unsigned int*
     }
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
-    const long long b = b0 + u * stride;
-    if (b >= nblocks) break;
-    float f[16];
-    {
-      float t[8];
-      unpack8(in[u][0], t);
+      const long long b = b0 + u * stride;
+      if (b >= nblocks) break;
+      const float amax = block_amax16(in[u][0], in[u][1]);
+      const float dec = __fmul_rn(__fdiv_rn(amax, 6.0f), s_enc);
+      const uint8_t sb = uint8_t(pack_e4m3x2(dec, 0.f) & 0xFF);
+      uint2 out = make_uint2(0u, 0u);   // a zero scale encodes every element as +0
+      if (sb != 0) {
+        const float sv = e4m3_to_float(sb);
+        const float y = __frcp_rn(sv);
+        const float2 nb = make_float2(-sv, -sv);
+        const float2 y2 = make_float2(y, y);
+        const uint32_t w[8] = {in[u][0].x, in[u][0].y, in[u][0].z, in[u][0].w,
+                               in[u][1].x, in[u][1].y, in[u][1].z, in[u][1].w};
+        float h[2][8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) f[j] = t[j];
-      unpack8(in[u][1], t);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) f[8 + j] = t[j];
-    }
-    float amax = 0.f;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(f[j]));
-    const float dec = __fmul_rn(__fdiv_rn(amax, 6.0f), s_enc);
-    const uint8_t sb = uint8_t(pack_e4m3x2(dec, 0.f) & 0xFF);
-    const float sv = e4m3_to_float(sb);
-    float q[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) q[j] = sv > 0.f ? __fdiv_rn(__fmul_rn(f[j], s_enc), sv) : 0.f;
-    float h0[8], h1[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      h0[j] = q[j];
-      h1[j] = q[8 + j];
-    }
-    packed[b] = make_uint2(pack_e2m1x8(h0), pack_e2m1x8(h1));
-    scales[b] = sb;
+        for (int i = 0; i < 8; ++i) {
+          const float2 a = __fmul2_rn(make_float2(bf16lo(w[i]), bf16hi(w[i])), s_enc2);
+          const float2 q = div2_by_block_scale(a, nb, y2);
+          h[i >> 2][2 * (i & 3)] = q.x;
+          h[i >> 2][2 * (i & 3) + 1] = q.y;
+        }
+        out = make_uint2(pack_e2m1x8(h[0]), pack_e2m1x8(h[1]));
+      }
+      packed[b] = out;
+      scales[b] = sb;
     }
   }
 }

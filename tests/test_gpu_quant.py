@@ -140,3 +140,26 @@ def test_nvfp4_rounding_ties_and_boundaries():
     rp, rs, re = oracle.nvfp4_quantize(x)
     assert np.array_equal(host(scales), rs)
     assert np.array_equal(host(packed), rp)
+
+
+def test_block_scale_division_is_correctly_rounded_exhaustively(tmp_path):
+    """The NVFP4 encoder divides by the block scale with one reciprocal per
+    block and a two-fma correction per element.  For every positive finite
+    E4M3 scale and every binary32 significand of dividends of both signs whose
+    quotient lies in [2^-3, 2^3) -- where every E2M1 decision is taken -- the
+    result must equal the compiler's correctly rounded division bit for bit
+    (the check kernel lives in tests/cuda and is built here)."""
+    import ctypes
+    import os
+    import subprocess
+    from bitwise_deterministic_moe_gb300 import build as B
+
+    here = os.path.dirname(os.path.abspath(__file__))
+    lib = str(tmp_path / "libblock_scale_check.so")
+    cmd = [B.nvcc()] + B._flags(["-I", B.CSRC]) + ["-shared", "-o", lib,
+                                                     os.path.join(here, "cuda", "block_scale_check.cu")]
+    subprocess.run(cmd, check=True, capture_output=True)
+    so = ctypes.CDLL(lib)
+    mism, first = ctypes.c_ulonglong(), ctypes.c_ulonglong()
+    assert so.block_scale_check(ctypes.byref(mism), ctypes.byref(first)) == 0
+    assert mism.value == 0, hex(first.value)
