@@ -575,6 +575,56 @@ def run_ours(args):
     return 0
 
 
+def dense_compare(args):
+    """The grouped GEMM on dense shapes (one expert holding every row, or equal
+    experts) next to cuBLAS (torch.matmul / torch.bmm) on the same bf16
+    operands: separates the kernel's own efficiency from the MoE routing.
+    Prints one JSON object; not part of the bench line."""
+    import torch
+    from bitwise_deterministic_moe_gb300 import api, build
+    build.build()
+    api.load()
+    torch.manual_seed(0)
+    res = {}
+    for E, Me, K, N in ((1, 131072, 1024, 2048), (64, 2048, 1024, 2048), (128, 1088, 1024, 2048)):
+        R = E * Me
+        X = torch.randn(R, K, device="cuda").to(torch.bfloat16)
+        W = (torch.randn(E, N, K, device="cuda") * 0.03).to(torch.bfloat16)
+        off = (torch.arange(E + 1, dtype=torch.int32, device="cuda") * Me).contiguous()
+        ws = api.workspace(R, 1, E)
+        out = torch.empty(R, N, dtype=torch.bfloat16, device="cuda")
+        ref = torch.empty(E, Me, N, dtype=torch.bfloat16, device="cuda")
+
+        def t(fn):
+            for _ in range(max(args.warmup, 3)):
+                fn()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(max(args.steps, 1)):
+                fn()
+            b.record()
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) / max(args.steps, 1)
+
+        if E == 1:
+            ms_ref = t(lambda: torch.matmul(X, W[0].t(), out=ref[0]))
+        else:
+            ms_ref = t(lambda: torch.bmm(X.view(E, Me, K), W.transpose(1, 2), out=ref))
+        ms_1 = t(lambda: api.grouped_gemm_fwd(X, W, off, ws, out=out, flags=api.LAUNCH_SINGLE_CTA))
+        same_1 = bool(torch.equal(out, ref.view(R, N)))
+        ms_2 = t(lambda: api.grouped_gemm_fwd(X, W, off, ws, out=out, flags=api.LAUNCH_CTA_PAIRS))
+        same_2 = bool(torch.equal(out, ref.view(R, N)))
+        fl = 2.0 * R * K * N
+        res[f"{E}x{Me}x{K}->{N}"] = {
+            "tflops": {"cublas": fl / ms_ref / 1e9, "single_cta": fl / ms_1 / 1e9, "cta_pairs": fl / ms_2 / 1e9},
+            "bitwise_equal_to_cublas": {"single_cta": same_1, "cta_pairs": same_2}}
+        del X, W, out, ref
+        torch.cuda.empty_cache()
+    print(json.dumps({"dense_compare": res}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -592,7 +642,11 @@ def main():
     ap.add_argument("--skip-dispatch", action="store_true")
     ap.add_argument("--skip-wgrad", action="store_true")
     ap.add_argument("--skip-quant", action="store_true")
+    ap.add_argument("--dense-compare", action="store_true",
+                    help="time the grouped GEMM on dense shapes next to cuBLAS and exit")
     args = ap.parse_args()
+    if args.dense_compare:
+        return dense_compare(args)
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     if args.impl == "reference":
