@@ -532,18 +532,23 @@ def run_ours(args):
     achieved_gbs = abytes / gemm_s / 1e9
     achieved_tf = flops / gemm_s / 1e12
     t_hbm = abytes / (pk["hbm_gbs"] * 1e9)
-    t_tc = flops / (pk["bf16_tflops"] * 1e12)
+    # the GEMM is timed inside a long run of back-to-back steps (the power
+    # limit engages), so its tensor peak is the sustained cuBLAS figure
+    tc_peak = pk.get("bf16_tflops_sustained") or FALLBACK_PEAKS["bf16_tflops_sustained"]
+    t_tc = flops / (tc_peak * 1e12)
     traffic = gemm_traffic_per_launch()
     if t_hbm >= t_tc:
         roof = {"bound": "hbm", "achieved": achieved_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved_gbs / pk["hbm_gbs"], "traffic": traffic}
     else:
-        roof = {"bound": "tensor", "achieved": achieved_tf, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": achieved_tf / pk["bf16_tflops"], "traffic": traffic}
+        roof = {"bound": "tensor", "achieved": achieved_tf, "peak": tc_peak, "unit": "TFLOP/s",
+                "frac": achieved_tf / tc_peak, "traffic": traffic}
     roof.update({"kernel": "grouped_gemm_kernel<slots> + combine (moe_grouped_gemm_dprob)",
                  "launch_ms": gemm_ms, "algorithmic_bytes": abytes, "algorithmic_flops": flops,
                  "peak_source": f"{pk_kind} ({PEAKS_FILE if pk_kind == 'measured' else 'profiling recipe'})",
-                 "tensor_frac": achieved_tf / pk["bf16_tflops"], "tensor_tflops": achieved_tf,
+                 "tensor_frac": achieved_tf / tc_peak, "tensor_tflops": achieved_tf,
+                 "tensor_peak": {"tflops": tc_peak, "kind": "sustained"},
+                 "tensor_frac_of_burst": achieved_tf / pk["bf16_tflops"],
                  "hbm_frac": achieved_gbs / pk["hbm_gbs"]})
     line = {
         "metric": "grouped-GEMM+dprob TFLOP/s", "value": value, "unit": "TFLOP/s", "n_gpus": world,
