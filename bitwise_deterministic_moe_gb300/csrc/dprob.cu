@@ -13,42 +13,64 @@ namespace {
 
 constexpr int SLOT = DMOE_SLOT_COLS;
 
-// One thread per (row r, slot s), r fastest so the slot stores coalesce.
-__global__ void __launch_bounds__(256)
+// A warp takes eight consecutive permuted rows and walks their slots.  Four
+// lanes share a row: lane k4 holds the 16-byte group k4 of each 64-byte
+// quarter of the slot (columns 32*ch + 8*k4 .. +7, ch = 0..3), so one load
+// instruction reads 64 contiguous bytes of each of eight rows of expert_out
+// (and of their tokens' grad_out rows).  Each lane chains its products over
+// ch, folds them with slot_tree, and two xor-shuffles give
+// (L0 + L1) + (L2 + L3): the fused epilogue's tree, so the bits are the same.
+// grad_out rows are read by every choice of their token (L2 evict-last);
+// expert_out streams through once (evict-first).
+constexpr int EPI_THREADS = 256;
+constexpr int EPI_ROWS_PER_WARP = 8;
+
+__global__ void __launch_bounds__(EPI_THREADS)
 dprob_epilogue_kernel(const uint16_t* __restrict__ grad_out, const uint16_t* __restrict__ expert_out,
                       const int32_t* __restrict__ offsets, const int32_t* __restrict__ row_src, int R, int E,
                       int topk, int N, int S, float* __restrict__ slots, int* status) {
   pdl_begin();
-  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= (long long)R * S) return;
-  const int s = int(idx / R);
-  const int r = int(idx - (long long)s * R);
+  const int lane = threadIdx.x & 31;
+  const int k4 = lane & 3;
+  const long long warp_id = ((long long)blockIdx.x * EPI_THREADS + threadIdx.x) >> 5;
   const int rows = offsets[E];
-  if (idx == 0 && rows != R) record_error(status, DMOE_ERR_ROUTING);
-  if (r >= rows) return;
-  const int src = row_src[r];
-  if (unsigned(src) >= unsigned(R)) {
-    record_error(status, DMOE_ERR_ROUTING);
-    return;
+  if (warp_id == 0 && lane == 0 && rows != R) record_error(status, DMOE_ERR_ROUTING);
+  const long long r0 = warp_id * EPI_ROWS_PER_WARP;
+  if (r0 >= R) return;                                   // whole warp
+  const int r = int(r0) + (lane >> 2);
+  bool ok = r < R && r < rows;
+  int tok = 0;
+  if (ok) {
+    const int src = row_src[r];
+    if (unsigned(src) >= unsigned(R)) {                  // corrupt row_src: report, never index with it
+      record_error(status, DMOE_ERR_ROUTING);
+      ok = false;
+    } else {
+      tok = src / topk;
+    }
   }
-  const int tok = src / topk;
-  const uint16_t* g = grad_out + size_t(tok) * N + size_t(s) * SLOT;
-  const uint16_t* y = expert_out + size_t(r) * N + size_t(s) * SLOT;
-  float part[4];
+  const uint16_t* g = grad_out + size_t(tok) * N + k4 * 8;
+  const uint16_t* y = expert_out + size_t(ok ? r : 0) * N + k4 * 8;
+  const uint64_t pol_keep = policy_evict_last();
+  const uint64_t pol_stream = policy_evict_first();
+#pragma unroll 2
+  for (int s = 0; s < S; ++s) {
+    uint4 gv[4], yv[4];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
+    for (int ch = 0; ch < 4; ++ch) {
+      gv[ch] = ok ? ldg_nc_v4_hint(g + s * SLOT + ch * 32, pol_keep) : make_uint4(0u, 0u, 0u, 0u);
+      yv[ch] = ok ? ldg_nc_v4_hint(y + s * SLOT + ch * 32, pol_stream) : make_uint4(0u, 0u, 0u, 0u);
+    }
     float a[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) a[j] = 0.0f;
 #pragma unroll
-    for (int gi = k; gi < SLOT / 8; gi += 4) {
-      const uint4 gv = ldg_nc_v4(g + gi * 8);
-      const uint4 yv = ldg_nc_v4(y + gi * 8);
-      slot_accumulate8(a, gv, yv);
-    }
-    part[k] = slot_tree(a);
+    for (int ch = 0; ch < 4; ++ch) slot_accumulate8(a, gv[ch], yv[ch]);
+    float part = slot_tree(a);
+    part = __fadd_rn(part, __shfl_xor_sync(0xffffffffu, part, 1));
+    part = __fadd_rn(part, __shfl_xor_sync(0xffffffffu, part, 2));
+    if (k4 == 0 && ok) slots[size_t(s) * R + r] = part;
   }
-  slots[size_t(s) * R + r] = slot_parts(part[0], part[1], part[2], part[3]);
 }
 
 // One thread per permuted row: ascending-slot fp32 sum, scattered to dprob.
@@ -82,10 +104,10 @@ cudaError_t launch_dprob_epilogue(const void* grad_out, const void* expert_out, 
                                   const int32_t* row_src, int R, int E, int topk, int N, float* slots,
                                   int* status, cudaStream_t stream) {
   const int S = N / SLOT;
-  const long long total = (long long)R * S;
-  if (total == 0) return cudaSuccess;
-  const unsigned grid = unsigned((total + 255) / 256);
-  return launch_chained(dprob_epilogue_kernel, dim3(grid), dim3(256), 0, stream,
+  if (R == 0 || S == 0) return cudaSuccess;
+  const long long warps = (R + EPI_ROWS_PER_WARP - 1) / EPI_ROWS_PER_WARP;
+  const unsigned grid = unsigned((warps * 32 + EPI_THREADS - 1) / EPI_THREADS);
+  return launch_chained(dprob_epilogue_kernel, dim3(grid), dim3(EPI_THREADS), 0, stream,
                         static_cast<const uint16_t*>(grad_out), static_cast<const uint16_t*>(expert_out), offsets,
                         row_src, R, E, topk, N, S, slots, status);
 }
