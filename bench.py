@@ -289,18 +289,23 @@ def wgrad_measure(api, cfg, X, dY, off, ws, timed, dev, iters):
             "tensor_frac": flops / (ms * 1e-3) / 1e12 / pk["bf16_tflops"]}
 
 
-def passes_measure(api, cfg, out, slots, src, timed, iters):
+def passes_measure(api, cfg, out, slots, src, off, G, timed, iters):
     """The HBM passes of the path on buffers of the workload: the chunk
-    fingerprint of expert_out (R*N*2 bytes, larger than L2) and the
-    fixed-order slot combine (slots S*R*4 read, row_src and dprob R*4 each)."""
+    fingerprint of expert_out (R*N*2 bytes, larger than L2), the fixed-order
+    slot combine (slots S*R*4 read, row_src and dprob R*4 each) and the
+    unfused slot epilogue (expert_out R*N*2 and row_src R*4 read, grad_out
+    T*N*2 read once, slots S*R*4 written)."""
     import torch
     pk, _ = peaks()
     fp = torch.empty(api.fingerprint_num_chunks(out.numel() * 2), dtype=torch.int64, device=out.device)
     dp = torch.empty(cfg.T, cfg.topk, dtype=torch.float32, device=out.device)
+    sl = torch.empty_like(slots)
     res = {}
     for name, fn, b in (("fingerprint_expert_out", lambda: api.fingerprint(out, out=fp), out.numel() * 2),
                         ("slot_combine", lambda: api.dprob_combine(slots, src, cfg.topk, dprob=dp),
-                         cfg.S * cfg.R * 4 + 2 * cfg.R * 4)):
+                         cfg.S * cfg.R * 4 + 2 * cfg.R * 4),
+                        ("unfused_epilogue", lambda: api.dprob_epilogue(G, out, off, src, cfg.topk, slots=sl),
+                         cfg.R * cfg.N * 2 + cfg.R * 4 + cfg.T * cfg.N * 2 + cfg.S * cfg.R * 4)):
         ms = timed(fn, iters)
         gbs = b / (ms * 1e-3) / 1e9
         res[name] = {"ms": ms, "algorithmic_bytes": b, "achieved_gbs": gbs, "peak_gbs": pk["hbm_gbs"],
@@ -496,7 +501,7 @@ def run_ours(args):
                                                               args.tax_iters)
     wg = None if args.skip_wgrad else wgrad_measure(api, cfg, X, out, off, ws, timed, dev, args.tax_iters)
     qz = None if args.skip_quant else quant_measure(api, X, ws, timed, args.tax_iters)
-    hp = passes_measure(api, cfg, out, slots, src, timed, args.tax_iters)
+    hp = passes_measure(api, cfg, out, slots, src, off, G, timed, max(args.tax_iters, 20))
 
     # ---------------- end to end through the public API, host buffers
     e2e = None
