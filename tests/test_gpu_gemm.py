@@ -162,6 +162,19 @@ def test_single_and_pair_kernels_bitwise_equal(name):
     assert api.read_status(prob.ws) == 0
 
 
+@pytest.mark.parametrize("name", ["latent", "imbal"])
+def test_unfused_epilogue_full_size_bitwise(name):
+    """The separate epilogue and combine launches give the fused call's slots
+    and dprob bit for bit at full size (every row, every slot)."""
+    prob = Problem(synth.CONFIGS[name])
+    out, dprob, slots = prob.run_dprob()
+    slots2 = api.dprob_epilogue(prob.G, out, prob.off, prob.src, prob.cfg.topk)
+    dprob2 = api.dprob_combine(slots2, prob.src, prob.cfg.topk)
+    assert api.read_status(prob.ws) == 0
+    assert torch.equal(slots.view(torch.int32), slots2.view(torch.int32))
+    assert torch.equal(dprob.view(torch.int32), dprob2.view(torch.int32))
+
+
 @pytest.mark.parametrize("num_ctas", [0, 37, 1])
 @pytest.mark.parametrize("cfg", SHAPES, ids=[c.name for c in SHAPES])
 def test_serialized_writers_bitwise_equal_to_slots(cfg, num_ctas):
