@@ -63,19 +63,26 @@ def algorithmic(cfg, off):
     return flops, bytes_
 
 
+def gemm_kernel_source_hash():
+    """sha256 (16 hex digits) of the device code of grouped_gemm.cu: the file up
+    to its host-side section, so launcher-only edits keep the capture valid."""
+    import hashlib
+    src = os.path.join(ROOT, "bitwise_deterministic_moe_gb300", "csrc", "grouped_gemm.cu")
+    text = open(src, encoding="utf-8").read()
+    marker = "// ---------------------------------------------------------------- host side"
+    return hashlib.sha256(text[:text.index(marker)].encode()).hexdigest()[:16]
+
+
 def gemm_traffic_per_launch():
     """dram read+write bytes of the GEMM kernel from the committed ncu summary,
-    or None when the kernel source changed after the capture."""
+    or None when the kernel's device code changed after the capture."""
     try:
-        import hashlib
         kv = {}
         for line in open(TRAFFIC_FILE):
             if "=" in line and not line.startswith("#"):
                 k, v = line.split("=", 1)
                 kv[k.strip()] = v.strip()
-        src = os.path.join(ROOT, "bitwise_deterministic_moe_gb300", "csrc", "grouped_gemm.cu")
-        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        if kv.get("kernel_source_sha256_16") != h:
+        if kv.get("kernel_device_code_sha256_16") != gemm_kernel_source_hash():
             return None
         return float(kv["dram_bytes_per_launch"])
     except Exception:
