@@ -83,6 +83,27 @@ def test_nvfp4_bytes_and_fingerprints(shape, seed, scale):
     assert ch == [int(c) for c in rch] and h == rh
 
 
+@pytest.mark.parametrize("shape", [(1, 16), (3, 48), (7, 80)])
+def test_nvfp4_signed_zeros_and_odd_block_counts(shape):
+    """Odd numbers of 16-value blocks (the encoder handles two per thread),
+    negative zeros, and negative values far below their block's maximum, whose
+    quotients round to -0: the encoder must keep the sign as IEEE division
+    does."""
+    rng = np.random.default_rng(sum(shape))
+    v = rng.standard_normal(shape).astype(np.float32)
+    v[:, 1::5] = -0.0
+    v[:, 2::7] = -1e-6 * np.abs(v[:, 2::7])
+    v[:, 3::11] = 1e-6 * np.abs(v[:, 3::11])
+    x = synth.f32_to_bf16_bits(v)
+    ws = api.workspace(1, 1, 1)
+    packed, scales, s_enc = api.quantize_nvfp4(bf16_dev(x), ws)
+    rp, rs, re = oracle.nvfp4_quantize(x)
+    assert np.array_equal(host(scales), rs)
+    assert np.array_equal(host(packed), rp)
+    assert host(s_enc).view(np.uint32)[0] == np.float32(re).view(np.uint32)
+    assert ((rp & 0xF) == 0x8).any() or ((rp >> 4) == 0x8).any()   # the case is exercised
+
+
 def test_nvfp4_zero_tensor_and_repeat():
     ws = api.workspace(1, 1, 1)
     z = torch.zeros(8, 64, dtype=torch.bfloat16, device="cuda")
