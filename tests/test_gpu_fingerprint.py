@@ -17,7 +17,8 @@ def _built():
 
 @pytest.mark.parametrize("nbytes,chunk", [(0, 1 << 20), (1, 16), (3, 16), (17, 16), (4096, 1024), (100003, 4096),
                                           ((1 << 20) + 5, 1 << 20), (3 * (1 << 20) + 12, 1 << 20),
-                                          (200000, 65536 * 3), (1 << 22, 1 << 22)])
+                                          (200000, 65536 * 3), (1 << 22, 1 << 22),
+                                          ((40 << 20) + 7, 4096)])   # 10,241 chunks: every cluster loops
 def test_positional_bit_exact(nbytes, chunk):
     data = np.random.default_rng(nbytes).integers(0, 256, nbytes, dtype=np.uint8)
     t = torch.from_numpy(data).cuda()
