@@ -73,16 +73,17 @@ def gemm_kernel_source_hash():
     return hashlib.sha256(text[:text.index(marker)].encode()).hexdigest()[:16]
 
 
-def gemm_traffic_per_launch():
-    """dram read+write bytes of the GEMM kernel from the committed ncu summary,
-    or None when the kernel's device code changed after the capture."""
+def gemm_traffic_per_launch(config):
+    """dram read+write bytes of the GEMM kernel from the committed ncu summary
+    of `config`, or None when there is none for it or the kernel's device code
+    changed after the capture."""
     try:
         kv = {}
         for line in open(TRAFFIC_FILE):
             if "=" in line and not line.startswith("#"):
                 k, v = line.split("=", 1)
                 kv[k.strip()] = v.strip()
-        if kv.get("kernel_device_code_sha256_16") != gemm_kernel_source_hash():
+        if kv.get("workload") != config or kv.get("kernel_device_code_sha256_16") != gemm_kernel_source_hash():
             return None
         return float(kv["dram_bytes_per_launch"])
     except Exception:
@@ -594,14 +595,16 @@ def run_ours(args):
     # limit engages), so its tensor peak is the sustained cuBLAS figure
     tc_peak = pk.get("bf16_tflops_sustained") or FALLBACK_PEAKS["bf16_tflops_sustained"]
     t_tc = flops / (tc_peak * 1e12)
-    traffic = gemm_traffic_per_launch()
+    traffic = gemm_traffic_per_launch(args.config)
     if t_hbm >= t_tc:
         roof = {"bound": "hbm", "achieved": achieved_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved_gbs / pk["hbm_gbs"], "traffic": traffic}
     else:
         roof = {"bound": "tensor", "achieved": achieved_tf, "peak": tc_peak, "unit": "TFLOP/s",
                 "frac": achieved_tf / tc_peak, "traffic": traffic}
-    roof.update({"kernel": "grouped_gemm_kernel<slots> + combine (moe_grouped_gemm_dprob)",
+    # the call's default kernel choice: CTA pairs when R >= 512*E (mean rows per expert)
+    gemm_kernel = "grouped_gemm_pair_kernel<slots>" if cfg.R >= 512 * cfg.E else "grouped_gemm_kernel<slots>"
+    roof.update({"kernel": gemm_kernel + " + combine (moe_grouped_gemm_dprob)",
                  "launch_ms": gemm_ms, "algorithmic_bytes": abytes, "algorithmic_flops": flops,
                  "peak_source": f"{pk_kind} ({PEAKS_FILE if pk_kind == 'measured' else 'profiling recipe'})",
                  "tensor_frac": achieved_tf / tc_peak, "tensor_tflops": achieved_tf,
