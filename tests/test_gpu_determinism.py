@@ -123,3 +123,48 @@ def test_relabel_and_token_permutation_bitwise():
     rows_base = flat0[torch.from_numpy(tj2).cuda()]
     rows_new = torch.from_numpy(inv2).cuda()
     assert torch.equal(out2.view(torch.int16)[rows_new], out0.view(torch.int16)[rows_base])
+
+
+@pytest.mark.parametrize("name", ["small", "latent"])
+def test_cuda_graph_replay_bitwise(name):
+    """The whole step (routing, fingerprint, GEMM + slots + combine,
+    fingerprint) captured once in a CUDA graph and replayed gives the eager
+    bits: every launch is graph-capturable (programmatic launches included)
+    and the workspace counters reset themselves between replays."""
+    cfg = synth.CONFIGS[name]
+    prob = Problem(cfg)
+    ids = torch.from_numpy(prob.inp.topk_ids).cuda()
+    off = torch.empty(cfg.E + 1, dtype=torch.int32, device="cuda")
+    src = torch.empty(cfg.R, dtype=torch.int32, device="cuda")
+    out = torch.empty(cfg.R, cfg.N, dtype=torch.bfloat16, device="cuda")
+    slots = torch.empty(cfg.S, cfg.R, dtype=torch.float32, device="cuda")
+    dprob = torch.empty(cfg.T, cfg.topk, dtype=torch.float32, device="cuda")
+    nch = api.fingerprint_num_chunks(cfg.R * 4)
+    fp_src = torch.empty(nch, dtype=torch.int64, device="cuda")
+    fp_dp = torch.empty(nch, dtype=torch.int64, device="cuda")
+
+    def step():
+        api.permute_indices(ids, cfg.E, prob.ws, off, src)
+        api.fingerprint(src, out=fp_src)
+        api.grouped_gemm_dprob(prob.X, prob.W, off, prob.G, src, cfg.topk, prob.ws, out=out, slots=slots,
+                               dprob=dprob)
+        api.fingerprint(dprob, out=fp_dp)
+
+    step()
+    torch.cuda.synchronize()
+    ref = [t.clone() for t in (off, src, out, slots, dprob, fp_src, fp_dp)]
+    for t in (off, src, out, slots, dprob, fp_src, fp_dp):
+        t.zero_()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            step()
+    torch.cuda.synchronize()
+    for _ in range(3):
+        g.replay()
+        torch.cuda.synchronize()
+        assert api.read_status(prob.ws) == 0
+        for a, b in zip(ref, (off, src, out, slots, dprob, fp_src, fp_dp)):
+            assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
