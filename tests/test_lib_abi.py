@@ -4,6 +4,7 @@ calls that are rejected before any CUDA call is made (no GPU needed)."""
 import ctypes
 import os
 import re
+import subprocess
 
 import pytest
 
@@ -131,3 +132,16 @@ def test_header_hash_matches_oracle_without_gpu(lib):
         h = ctypes.c_uint64()
         assert fp(None, 0, code, len(shape), arr, 1 << 20, 0, None, ctypes.byref(h), None) == 0
         assert h.value == oracle.header_hash(code, shape)
+
+
+def test_header_is_c99_and_the_library_links_from_c(lib, tmp_path):
+    """A plain C99 program includes the header (-std=c99 -pedantic -Werror),
+    links libdmoe.so and calls the entry points that need no GPU."""
+    here = os.path.dirname(os.path.abspath(__file__))
+    libdir = os.path.dirname(build.LIB)
+    exe = str(tmp_path / "abi_consumer")
+    subprocess.run(["gcc", "-std=c99", "-pedantic", "-Wall", "-Wextra", "-Werror",
+                    "-I", os.path.join(build.ROOT, "include"), os.path.join(here, "c", "abi_consumer.c"),
+                    "-L", libdir, "-ldmoe", "-Wl,-rpath," + libdir, "-o", exe], check=True)
+    res = subprocess.run([exe], capture_output=True, text=True, check=True)
+    assert res.stdout.strip() == "ok"
