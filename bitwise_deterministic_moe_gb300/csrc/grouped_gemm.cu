@@ -143,7 +143,7 @@ __device__ __forceinline__ Tile decode_tile(int t, const Ctrl& c, int E, int NT,
 template <int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                    const KParams p) {
+                    const __grid_constant__ CUtensorMap tmap_o, const KParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Ctrl& c = *reinterpret_cast<Ctrl*>(base + size_t(STAGES) * STAGE_BYTES + size_t(EPI_WARPS) * STG_BYTES);
@@ -359,6 +359,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
         ok[i] = active && rr[i] < tl.row_end;
         src[i] = 0;
       }
+      // a warp whose 32 rows all belong to the expert writes each 32x32 chunk
+      // with one TMA tensor store from the staging buffer; a ragged last
+      // quarter (rows of the next expert follow) stores row by row instead
+      const bool full32 = active && (tl.row0 + q * 32 + 32 <= tl.row_end);
       // Prefetch grad_out for all four rows before the accumulator is ready.
       uint4 g[16];
       if (MODE != int(GemmMode::kFwd)) {
@@ -393,7 +397,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
           uint32_t v[32];
           tmem_ld_32x32b_x32(tcol + uint32_t(ch * 32), v);
           tmem_wait_ld();
+          // the previous chunk's tensor store must have read the staging buffer
+          if (lane == 0) bulk_wait_group_read<0>();
+          __syncwarp();
           // row `lane` of the chunk -> staging, piece kk at slot kk ^ ((row >> 1) & 3)
+          // (the 64-byte swizzle of the output tensor map)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             uint4 y;
@@ -404,12 +412,20 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
             sts_v4(stg + uint32_t(lane * 64 + ((kk ^ ((lane >> 1) & 3)) << 4)), y);
           }
           __syncwarp();
+          if (full32) {
+            fence_proxy_async_smem();   // the generic-proxy staging writes, before the TMA unit reads them
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmap_o, stg, col0 + ch * 32, tl.row0 + q * 32);
+              bulk_commit_group();
+            }
+          }
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int row = i * 8 + (lane >> 2);
             const uint4 y = lds_v4(stg + uint32_t(row * 64 + ((k4 ^ ((row >> 1) & 3)) << 4)));
             if (ok[i]) {
-              stg_v4(p.out + size_t(rr[i]) * p.N + col0 + ch * 32 + k4 * 8, y);
+              if (!full32) stg_v4(p.out + size_t(rr[i]) * p.N + col0 + ch * 32 + k4 * 8, y);
               if (MODE != int(GemmMode::kFwd)) slot_accumulate8(a[i], g[ch * 4 + i], y);
             }
           }
@@ -462,6 +478,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
       if (lane == 0) mbar_arrive(smem_u32(&c.acc_empty[acc]));
       if (++acc == ACC_BUFS) { acc = 0; aph ^= 1u; }
     }
+    // every tensor store of this warp has landed before the CTA can exit
+    if (lane == 0) bulk_wait_group_all();
   }
 
   __syncthreads();
@@ -516,6 +534,20 @@ bool make_tmap_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t col
   return r == CUDA_SUCCESS;
 }
 
+// 2-D bf16 output [rows, cols] (cols contiguous, cols % 8 == 0) for TMA stores of
+// box [32, 32] (64-byte rows) from a 64-byte-swizzled staging buffer.
+bool make_tmap_bf16_store32(CUtensorMap* m, void* ptr, uint64_t rows, uint64_t cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {32u, 32u};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // 2-D fp32 tensor [rows, cols] (cols contiguous, cols % 4 == 0) for TMA stores of
 // box [box_rows, 16] through a 64-byte-swizzled staging buffer.
 bool make_tmap_f32_store(CUtensorMap* m, void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
@@ -533,11 +565,11 @@ bool make_tmap_f32_store(CUtensorMap* m, void* ptr, uint64_t rows, uint64_t cols
 namespace {
 
 template <int MODE>
-cudaError_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const KParams& kp, int grid,
-                        cudaStream_t stream) {
+cudaError_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to, const KParams& kp,
+                        int grid, cudaStream_t stream) {
   const cudaError_t e = ensure_kernel_smem(reinterpret_cast<const void*>(grouped_gemm_kernel<MODE>), int(kSmemBytes));
   if (e != cudaSuccess) return e;
-  return launch_chained(grouped_gemm_kernel<MODE>, dim3(grid), dim3(NUM_THREADS), kSmemBytes, stream, ta, tb, kp);
+  return launch_chained(grouped_gemm_kernel<MODE>, dim3(grid), dim3(NUM_THREADS), kSmemBytes, stream, ta, tb, to, kp);
 }
 
 }  // namespace
@@ -549,9 +581,10 @@ size_t serial_flag_bytes(long long R, int E) {
 
 cudaError_t launch_grouped_gemm_1sm(GemmMode mode, const GemmArgs& a, cudaStream_t stream) {
   if (a.R == 0) return cudaSuccess;
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, to;
   if (!make_tmap_bf16(&ta, a.X, uint64_t(a.R), uint64_t(a.K), BM)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16(&tb, a.W, uint64_t(a.E) * a.N, uint64_t(a.K), BN)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16_store32(&to, a.out, uint64_t(a.R), uint64_t(a.N))) return cudaErrorInvalidValue;
   KParams kp;
   kp.offsets = a.offsets;
   kp.E = a.E;
@@ -575,10 +608,10 @@ cudaError_t launch_grouped_gemm_1sm(GemmMode mode, const GemmArgs& a, cudaStream
   int grid = a.num_ctas > 0 ? a.num_ctas : device_sm_count();
   if (mode == GemmMode::kSerial && !kp.wflags) return cudaErrorInvalidValue;
   switch (mode) {
-    case GemmMode::kFwd: return launch_mode<int(GemmMode::kFwd)>(ta, tb, kp, grid, stream);
-    case GemmMode::kSlots: return launch_mode<int(GemmMode::kSlots)>(ta, tb, kp, grid, stream);
-    case GemmMode::kAtomic: return launch_mode<int(GemmMode::kAtomic)>(ta, tb, kp, grid, stream);
-    case GemmMode::kSerial: return launch_mode<int(GemmMode::kSerial)>(ta, tb, kp, grid, stream);
+    case GemmMode::kFwd: return launch_mode<int(GemmMode::kFwd)>(ta, tb, to, kp, grid, stream);
+    case GemmMode::kSlots: return launch_mode<int(GemmMode::kSlots)>(ta, tb, to, kp, grid, stream);
+    case GemmMode::kAtomic: return launch_mode<int(GemmMode::kAtomic)>(ta, tb, to, kp, grid, stream);
+    case GemmMode::kSerial: return launch_mode<int(GemmMode::kSerial)>(ta, tb, to, kp, grid, stream);
   }
   return cudaErrorInvalidValue;
 }
