@@ -34,6 +34,7 @@
 namespace dmoe {
 
 bool make_tmap_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows);
+bool make_tmap_bf16_store32(CUtensorMap* m, void* ptr, uint64_t rows, uint64_t cols);
 
 namespace {
 
@@ -160,7 +161,7 @@ __device__ __forceinline__ bool pwarp_wait(uint32_t bar, uint32_t parity, Ctrl& 
 template <int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                         const KParams p) {
+                         const __grid_constant__ CUtensorMap tmap_o, const KParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Ctrl& c = *reinterpret_cast<Ctrl*>(base + size_t(STAGES) * STAGE_BYTES + size_t(EPI_WARPS) * STG_BYTES);
@@ -415,6 +416,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
         ok[i] = active && rr[i] < tl.row_end;
         src[i] = 0;
       }
+      // full 32-row quarters leave through TMA tensor stores of the staging
+      // buffer; a ragged quarter at the expert's end stores row by row
+      const bool full32 = active && (row_cta + q * 32 + 32 <= tl.row_end);
       uint4 g[16];
       if (MODE != int(GemmMode::kFwd)) {
 #pragma unroll
@@ -448,6 +452,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
           uint32_t v[32];
           tmem_ld_32x32b_x32(tcol + uint32_t(ch * 32), v);
           tmem_wait_ld();
+          if (lane == 0) bulk_wait_group_read<0>();   // the previous chunk's store has read the staging
+          __syncwarp();
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             uint4 y;
@@ -458,12 +464,20 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
             sts_v4(stg + uint32_t(lane * 64 + ((kk ^ ((lane >> 1) & 3)) << 4)), y);
           }
           __syncwarp();
+          if (full32) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmap_o, stg, col0 + ch * 32, row_cta + q * 32);
+              bulk_commit_group();
+            }
+          }
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int row = i * 8 + (lane >> 2);
             const uint4 y = lds_v4(stg + uint32_t(row * 64 + ((k4 ^ ((row >> 1) & 3)) << 4)));
             if (ok[i]) {
-              stg_v4(p.out + size_t(rr[i]) * p.N + col0 + ch * 32 + k4 * 8, y);
+              if (!full32) stg_v4(p.out + size_t(rr[i]) * p.N + col0 + ch * 32 + k4 * 8, y);
               if (MODE != int(GemmMode::kFwd)) slot_accumulate8(a[i], g[ch * 4 + i], y);
             }
           }
@@ -491,6 +505,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
       }
       if (++acc == ACC_BUFS) { acc = 0; aph ^= 1u; }
     }
+    if (lane == 0) bulk_wait_group_all();   // this warp's tensor stores have landed
   }
 
   // No CTA leaves (or frees tensor memory) while the other may still touch
@@ -513,7 +528,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
 }
 
 template <int MODE>
-cudaError_t launch_pair_mode(const CUtensorMap& ta, const CUtensorMap& tb, const KParams& kp, int grid,
+cudaError_t launch_pair_mode(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to, const KParams& kp,
+                             int grid,
                              cudaStream_t stream) {
   const cudaError_t e =
       ensure_kernel_smem(reinterpret_cast<const void*>(grouped_gemm_pair_kernel<MODE>), int(kSmemBytes));
@@ -532,7 +548,7 @@ cudaError_t launch_pair_mode(const CUtensorMap& ta, const CUtensorMap& tb, const
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<MODE>, ta, tb, kp);
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<MODE>, ta, tb, to, kp);
 }
 
 // Largest even CTA count whose pairs can all be resident at once (per device).
@@ -570,6 +586,8 @@ cudaError_t launch_pairs(const GemmArgs& a, cudaStream_t stream) {
   CUtensorMap ta, tb;
   if (!make_tmap_bf16(&ta, a.X, uint64_t(a.R), uint64_t(a.K), BM)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16(&tb, a.W, uint64_t(a.E) * a.N, uint64_t(a.K), BNH)) return cudaErrorInvalidValue;
+  CUtensorMap to;
+  if (!make_tmap_bf16_store32(&to, a.out, uint64_t(a.R), uint64_t(a.N))) return cudaErrorInvalidValue;
   KParams kp;
   kp.offsets = a.offsets;
   kp.E = a.E;
@@ -594,7 +612,7 @@ cudaError_t launch_pairs(const GemmArgs& a, cudaStream_t stream) {
   grid = grid < resident ? grid : resident;    // every pair resident: no pair waits on a queued one
   grid &= ~1;
   if (grid < 2) grid = 2;
-  return launch_pair_mode<MODE>(ta, tb, kp, grid, stream);
+  return launch_pair_mode<MODE>(ta, tb, to, kp, grid, stream);
 }
 
 }  // namespace
