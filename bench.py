@@ -65,12 +65,19 @@ def algorithmic(cfg, off):
 
 def gemm_kernel_source_hash():
     """sha256 (16 hex digits) of the device code of grouped_gemm.cu: the file up
-    to its host-side section, so launcher-only edits keep the capture valid."""
+    to its host-side section, without comments and layout, so launcher-only or
+    comment-only edits keep the capture valid."""
     import hashlib
+    import re
     src = os.path.join(ROOT, "bitwise_deterministic_moe_gb300", "csrc", "grouped_gemm.cu")
     text = open(src, encoding="utf-8").read()
     marker = "// ---------------------------------------------------------------- host side"
-    return hashlib.sha256(text[:text.index(marker)].encode()).hexdigest()[:16]
+    code = text[:text.index(marker)]
+    # comments and layout do not change the kernel
+    code = re.sub(r"/\*.*?\*/", " ", code, flags=re.S)
+    code = re.sub(r"//[^\n]*", " ", code)
+    code = " ".join(code.split())
+    return hashlib.sha256(code.encode()).hexdigest()[:16]
 
 
 def gemm_traffic_per_launch(config):

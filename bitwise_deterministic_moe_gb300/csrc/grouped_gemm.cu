@@ -15,11 +15,13 @@
 //           per stage, 128-byte swizzle, 4-stage ring in shared memory.
 //   warp 1  tcgen05.mma issuer (one thread): 128x256x16 bf16 MMAs, fp32
 //           accumulators in tensor memory, double-buffered (2 x 256 columns).
-//   warps 2-9  epilogue: tcgen05.ld of the accumulator, bf16 rounding, masked
-//           stores of expert_out rows, and the per-slot dot products with
-//           grad_out in the fixed tree (one thread per output row; one warp
-//           per 32 rows x 128 columns = one private slot).  The row's
-//           grad_out slice is fetched before the accumulator is ready.
+//   warps 2-9  epilogue: tcgen05.ld of the accumulator, bf16 rounding into a
+//           swizzled staging buffer, expert_out stores (a TMA tensor store per
+//           32x32 chunk when all 32 rows belong to the expert, masked row
+//           stores otherwise), and the per-slot dot products with grad_out in
+//           the fixed tree (one warp per 32 rows x 128 columns = one private
+//           slot).  The rows' grad_out slices are fetched before the
+//           accumulator is ready.
 // Tiles (one m-tile x one n-tile of one expert) are ordered so that heavy and
 // light experts' work interleaves (see decode_tile) and handed out dynamically
 // through a global counter: each output element is produced by exactly one
