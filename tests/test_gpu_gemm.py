@@ -33,6 +33,11 @@ LARGE = [
     synth.custom_config("wideN", T=96, E=4, topk=2, K=128, N=8192, index=307),
     synth.custom_config("deepK", T=160, E=8, topk=3, K=8192, N=256, index=308),
     synth.custom_config("bigW", T=256, E=1024, topk=2, K=4096, N=512, index=309),  # W = 4 GiB
+    # the documented extremes: K = 8 (one 8-column slice, the rest of the box
+    # zero-filled), K = 65536 (1024 k-blocks), N = 65536 (256 n-tiles, 512 slots)
+    synth.custom_config("k8", T=200, E=3, topk=2, K=8, N=256, index=311),
+    synth.custom_config("k64k", T=40, E=2, topk=1, K=65536, N=128, index=312),
+    synth.custom_config("n64k", T=24, E=2, topk=2, K=64, N=65536, index=313),
 ]
 
 
