@@ -82,6 +82,10 @@ SHAPES = [
     synth.custom_config("zipf", T=1024, E=64, topk=6, K=256, N=512, routing="zipf", index=304),
     synth.custom_config("n128", T=400, E=6, topk=2, K=192, N=128, index=306),
     synth.custom_config("deepN", T=64, E=3, topk=2, K=64, N=8192, index=310),
+    # the documented extremes: K = 8, K = 65536, N = 65536
+    synth.custom_config("wk8", T=200, E=3, topk=2, K=8, N=256, index=314),
+    synth.custom_config("wk64k", T=40, E=2, topk=1, K=65536, N=128, index=315),
+    synth.custom_config("wn64k", T=24, E=2, topk=2, K=64, N=65536, index=316),
 ]
 
 
