@@ -63,6 +63,7 @@ GATHER_SHAPES = [
     (synth.custom_config("g136", T=129, E=7, topk=3, K=16, N=136, index=402), "17 vectors: ragged lanes"),
     (synth.custom_config("g2048", T=300, E=16, topk=6, K=16, N=2048, index=403), "one full chunk per lane"),
     (synth.custom_config("g4104", T=70, E=5, topk=4, K=16, N=4104, index=404), "513 vectors: chunk tail"),
+    (synth.custom_config("g65536", T=20, E=3, topk=2, K=16, N=65536, index=405), "H at the limit: 32 chunks"),
 ]
 
 
@@ -84,6 +85,7 @@ COMBINE_SHAPES = [
     synth.custom_config("c384", T=64, E=8, topk=3, K=16, N=384, index=414),      # 48 vectors, 2 warps
     synth.custom_config("c2056", T=50, E=40, topk=22, K=16, N=2056, index=415),  # 257 vectors, 8 warps + tail
     synth.custom_config("c64", T=20, E=70, topk=64, K=16, N=256, index=416),     # topk at the limit
+    synth.custom_config("c65536", T=16, E=6, topk=3, K=16, N=65536, index=417),  # N at the limit
 ]
 
 
