@@ -46,7 +46,7 @@ Contents and the passage each part follows:
   "positional" hashes raw bits with position mixing; mode "xor" reduces each
   chunk the way ``torch.hash_tensor`` reduces a tensor.
 
-The hash is this build's own definition (the pages name only the
+The hash is the library's own definition (the pages name only the
 ``torch.hash_tensor`` xor reduction):
     fmix32  -- MurmurHash3's 32-bit finalizer (A. Appleby, public domain)
     sm64    -- the splitmix64 output function (Steele, Lea, Flood 2014)

@@ -4,7 +4,7 @@ The pages ("NVIDIA fait passer le déterminisme bit à bit de Megatron Core à
 2432 GPU ...", section "Méthodologie de débogage du non-déterminisme")
 fingerprint tensors on the GPU with torch.hash_tensor, record shape, dtype and
 element count, and hash order-sensitive data chunk by chunk.  The positional
-mode is this build's definition (see the oracle's header); it is pinned by the
+mode is the library's own definition (see the oracle's header); it is pinned by the
 published vectors of its two mixing functions, by a second, independent
 pure-Python implementation, and by the properties a chunk fingerprint must
 have.  The xor mode is pinned against the library routine torch.hash_tensor.
