@@ -41,6 +41,7 @@ WORKLOAD = "latent"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "grouped_gemm_latent_traffic.txt")
+KERNEL_FLAGS = {"auto": 0, "single": 2, "pairs": 4}   # the C ABI's DMOE_LAUNCH_SINGLE_CTA / _CTA_PAIRS
 
 
 def peaks():
@@ -407,7 +408,8 @@ def run_ours(args):
         api.fingerprint(src, out=fp_src)
         if ev is not None:
             ev[0].record(stream)
-        api.grouped_gemm_dprob(X_, W, off, G_, src, k, ws, out=out, slots=slots, dprob=dprob)
+        api.grouped_gemm_dprob(X_, W, off, G_, src, k, ws, out=out, slots=slots, dprob=dprob,
+                               num_ctas=args.num_ctas, flags=KERNEL_FLAGS[args.kernel])
         if ev is not None:
             ev[1].record(stream)
         api.fingerprint(dprob, out=fp_dp)
@@ -613,7 +615,8 @@ def run_ours(args):
         roof = {"bound": "tensor", "achieved": achieved_tf, "peak": tc_peak, "unit": "TFLOP/s",
                 "frac": achieved_tf / tc_peak, "traffic": traffic}
     # the call's default kernel choice: CTA pairs when R >= 512*E (mean rows per expert)
-    gemm_kernel = "grouped_gemm_pair_kernel<slots>" if cfg.R >= 512 * cfg.E else "grouped_gemm_kernel<slots>"
+    pairs = args.kernel == "pairs" or (args.kernel == "auto" and cfg.R >= 512 * cfg.E)
+    gemm_kernel = "grouped_gemm_pair_kernel<slots>" if pairs else "grouped_gemm_kernel<slots>"
     roof.update({"kernel": gemm_kernel + " + combine (moe_grouped_gemm_dprob)",
                  "launch_ms": gemm_ms, "algorithmic_bytes": abytes, "algorithmic_flops": flops,
                  "peak_source": f"{pk_kind} ({PEAKS_FILE if pk_kind == 'measured' else 'profiling recipe'})",
@@ -631,7 +634,8 @@ def run_ours(args):
                    "l2": "inputs larger than L2 (X+W+grad_out = %.2f GB)" % ((cfg.R * cfg.K + cfg.E * cfg.N * cfg.K
                                                                             + cfg.T * cfg.N) * 2 / 1e9),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "maxvio": synth.maxvio(inp.topk_ids, cfg.E)},
+                   "maxvio": synth.maxvio(inp.topk_ids, cfg.E),
+                   "gemm_launch": {"kernel": gemm_kernel, "num_ctas": args.num_ctas or "all resident"}},
         "gpu_launches": launches_per_step * args.steps,
         "roofline": roof,
         "determinism_tax": tax,
@@ -718,6 +722,9 @@ def main():
     ap.add_argument("--skip-dispatch", action="store_true")
     ap.add_argument("--skip-wgrad", action="store_true")
     ap.add_argument("--skip-quant", action="store_true")
+    ap.add_argument("--num-ctas", type=int, default=0, help="persistent CTAs of the GEMM (0 = all resident)")
+    ap.add_argument("--kernel", default="auto", choices=sorted(KERNEL_FLAGS),
+                    help="GEMM kernel: the call's own choice, or force one (same bits)")
     ap.add_argument("--dense-compare", action="store_true",
                     help="time the grouped GEMM on dense shapes next to cuBLAS and exit")
     args = ap.parse_args()
