@@ -74,6 +74,7 @@ dprob_epilogue_kernel(const uint16_t* __restrict__ grad_out, const uint16_t* __r
 }
 
 // One thread per permuted row: ascending-slot fp32 sum, scattered to dprob.
+// The general form, for any R, S and alignment.
 template <int S_STATIC>
 __global__ void __launch_bounds__(256)
 dprob_combine_kernel(const float* __restrict__ slots, const int32_t* __restrict__ row_src, int R, int S,
@@ -98,6 +99,50 @@ dprob_combine_kernel(const float* __restrict__ slots, const int32_t* __restrict_
   if (unsigned(dst) < unsigned(R)) dprob[dst] = acc;   // a corrupt index is skipped, never written through
 }
 
+// The vectorised form (R % 4 == 0, slots and row_src 16-byte aligned): a
+// thread owns four consecutive rows and reads each slot's four values with
+// one 16-byte load, all of its S loads in flight at once, so the pass moves
+// the slot buffer in few, wide requests.  Each row is still summed on its own
+// in ascending s from slot 0, so the bits equal the general form's.
+template <int S_STATIC>
+__global__ void __launch_bounds__(256)
+dprob_combine_v4_kernel(const float* __restrict__ slots, const int32_t* __restrict__ row_src, int R, int S,
+                        float* __restrict__ dprob) {
+  pdl_begin();
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;   // group of rows 4i .. 4i+3
+  if (4ll * i >= R) return;
+  const int nS = S_STATIC > 0 ? S_STATIC : S;
+  const float4* p = reinterpret_cast<const float4*>(slots) + i;
+  const size_t stride = size_t(R) / 4;                   // one slot, in float4
+  float4 acc = __ldg(p);
+  if (S_STATIC > 0) {
+    float4 v[S_STATIC > 1 ? S_STATIC - 1 : 1];
+#pragma unroll
+    for (int s = 1; s < nS; ++s) v[s - 1] = __ldg(p + size_t(s) * stride);
+#pragma unroll
+    for (int s = 1; s < nS; ++s) {
+      acc.x = __fadd_rn(acc.x, v[s - 1].x);
+      acc.y = __fadd_rn(acc.y, v[s - 1].y);
+      acc.z = __fadd_rn(acc.z, v[s - 1].z);
+      acc.w = __fadd_rn(acc.w, v[s - 1].w);
+    }
+  } else {
+    for (int s = 1; s < nS; ++s) {
+      const float4 v = __ldg(p + size_t(s) * stride);
+      acc.x = __fadd_rn(acc.x, v.x);
+      acc.y = __fadd_rn(acc.y, v.y);
+      acc.z = __fadd_rn(acc.z, v.z);
+      acc.w = __fadd_rn(acc.w, v.w);
+    }
+  }
+  const int4 dst = __ldg(reinterpret_cast<const int4*>(row_src) + i);
+  // a corrupt index is skipped, never written through
+  if (unsigned(dst.x) < unsigned(R)) dprob[dst.x] = acc.x;
+  if (unsigned(dst.y) < unsigned(R)) dprob[dst.y] = acc.y;
+  if (unsigned(dst.z) < unsigned(R)) dprob[dst.z] = acc.z;
+  if (unsigned(dst.w) < unsigned(R)) dprob[dst.w] = acc.w;
+}
+
 }  // namespace
 
 cudaError_t launch_dprob_epilogue(const void* grad_out, const void* expert_out, const int32_t* offsets,
@@ -115,6 +160,16 @@ cudaError_t launch_dprob_epilogue(const void* grad_out, const void* expert_out, 
 cudaError_t launch_dprob_combine(const float* slots, const int32_t* row_src, int R, int S, float* dprob,
                                  cudaStream_t stream) {
   if (R == 0) return cudaSuccess;
+  const bool v4 = R % 4 == 0 && ((reinterpret_cast<uintptr_t>(slots) | reinterpret_cast<uintptr_t>(row_src)) & 15) == 0;
+  if (v4) {
+    const unsigned grid = unsigned((R / 4 + 255) / 256);
+    switch (S) {
+      case 1: return launch_chained(dprob_combine_v4_kernel<1>, dim3(grid), dim3(256), 0, stream, slots, row_src, R, S, dprob);
+      case 2: return launch_chained(dprob_combine_v4_kernel<2>, dim3(grid), dim3(256), 0, stream, slots, row_src, R, S, dprob);
+      case 16: return launch_chained(dprob_combine_v4_kernel<16>, dim3(grid), dim3(256), 0, stream, slots, row_src, R, S, dprob);
+      default: return launch_chained(dprob_combine_v4_kernel<0>, dim3(grid), dim3(256), 0, stream, slots, row_src, R, S, dprob);
+    }
+  }
   const unsigned grid = unsigned((R + 255) / 256);
   switch (S) {
     case 1: return launch_chained(dprob_combine_kernel<1>, dim3(grid), dim3(256), 0, stream, slots, row_src, R, S, dprob);

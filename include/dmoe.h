@@ -296,12 +296,18 @@ dmoe_status moe_grouped_gemm_dprob_serial(const void* X_perm, const void* W, con
  * loads the library until the process exits), and no workspace is taken.
  *  - S * R > DMOE_NOALLOC_MAX_SLOT_VALUES returns DMOE_ERR_UNSUPPORTED.
  *  - Allocates nothing: no cudaMalloc/cudaFree, no allocating library call.
- *  - The first call on a device looks up the array's device address
- *    (cudaGetSymbolAddress, with that device current); make that first call
- *    before any stream capture.
+ *  - The first call in each CUDA context (once per device, and again after
+ *    cudaDeviceReset or under a context created by other code) looks up the
+ *    array's device address (cudaGetSymbolAddress, with that device current)
+ *    and caches it under the context's id; make that first call before any
+ *    stream capture.
  *  - All calls share the one array and it keeps the last call's contents
  *    (nothing in it needs to start at zero); calls whose work overlaps on
- *    the GPU (other streams, other threads) race on it.
+ *    the GPU (other streams, other threads) race on it and on the GEMM's
+ *    tile counters, and their outputs are undefined.  Each call clears those
+ *    two counters on its stream (an 8-byte cudaMemsetAsync, no allocation)
+ *    before its GEMM starts, so a race never affects later calls that are
+ *    ordered on one stream.
  *  - Device-side errors (bad routing data, a timed-out wait) are not
  *    recorded; outputs are then undefined.  Use moe_grouped_gemm_dprob with a
  *    workspace to have them reported.

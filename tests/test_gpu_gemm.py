@@ -139,18 +139,20 @@ def test_zero_rows():
     assert out.shape == (0, 256)
 
 
-@pytest.mark.parametrize("flags", [0] + KERNELS, ids=["default"] + KERNEL_IDS)
-@pytest.mark.parametrize("name", ["small", "latent", "imbal"])
-def test_full_size_sampled_rows(name, flags):
+@pytest.mark.parametrize("name", ["small", "latent", "imbal", "stress"])
+def test_full_size_sampled_rows(name):
     """Full size, in the benchmark's launch configuration (flags 0) and with
-    each kernel forced, on sampled rows the oracle computes one by one."""
+    each kernel forced, on sampled rows the oracle computes one by one, with
+    the per-element bound on slots and dprob."""
     cfg = synth.CONFIGS[name]
     prob = Problem(cfg)
-    out, dprob, slots = prob.run_dprob(flags=flags)
-    assert api.read_status(prob.ws) == 0
     off = prob.off.cpu().numpy()
     rows = gpu_util.sample_rows(off, 96, seed=cfg.seed)
-    gpu_util.check_rows_against_oracle(prob, out, slots, dprob, rows)
+    for flags in [0] + KERNELS:
+        out, dprob, slots = prob.run_dprob(flags=flags)
+        assert api.read_status(prob.ws) == 0
+        gpu_util.check_rows_against_oracle(prob, out, slots, dprob, rows)
+        del out, dprob, slots
 
 
 @pytest.mark.parametrize("name", ["tiny", "small", "latent", "imbal"])
@@ -217,3 +219,36 @@ def test_large_dimensions(cfg, flags):
     assert api.read_status(prob.ws) == 0
     off = prob.off.cpu().numpy()
     gpu_util.check_rows_against_oracle(prob, out, slots, dprob, gpu_util.sample_rows(off, 48, seed=cfg.seed))
+
+
+@pytest.mark.parametrize("R,S", [(4096, 16), (4097, 16), (1803, 2), (2048, 5), (1000, 1)])
+@pytest.mark.parametrize("aligned", [True, False], ids=["aligned", "offset_views"])
+def test_combine_vector_and_general_forms(R, S, aligned):
+    """The fixed-order combine is defined as an fp32 left-to-right sum over
+    ascending slots, scattered through row_src.  Both kernel forms (four rows
+    per thread with 16-byte loads when R % 4 == 0 and the buffers are 16-byte
+    aligned; one row per thread otherwise, here forced by R % 4 != 0 or by
+    views that start 4 bytes into their buffers) must give exactly those bits."""
+    g = torch.Generator().manual_seed(R * 31 + S)
+    sl_h = (torch.randn(S, R, generator=g) * torch.exp(torch.randn(S, R, generator=g) * 3)).float()
+    src_h = torch.randperm(R, generator=g).to(torch.int32)
+    if aligned:
+        sl = sl_h.cuda()
+        src = src_h.cuda()
+    else:
+        sl_buf = torch.empty(S * R + 1, dtype=torch.float32, device="cuda")
+        sl = sl_buf[1:].view(S, R)
+        sl.copy_(sl_h)
+        src_buf = torch.empty(R + 1, dtype=torch.int32, device="cuda")
+        src = src_buf[1:]
+        src.copy_(src_h)
+    dprob = api.dprob_combine(sl, src, 1)
+    torch.cuda.synchronize()
+    a = sl_h.numpy()
+    acc = a[0].copy()
+    for s in range(1, S):
+        acc = (acc + a[s]).astype(np.float32)      # IEEE fp32 addition, round to nearest even
+    want = np.empty(R, np.float32)
+    want[src_h.numpy()] = acc
+    got = dprob.reshape(-1).cpu().numpy()
+    assert np.array_equal(got.view(np.int32), want.view(np.int32))
