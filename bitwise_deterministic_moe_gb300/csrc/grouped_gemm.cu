@@ -10,7 +10,7 @@
 // output columns, independent of the MMA tile width, so the bits do not
 // depend on the tile shape either.
 //
-// Design (one CTA per SM, persistent, warp-specialised, 320 threads):
+// Design (one CTA per SM, persistent, warp-specialised, 352 threads):
 //   warp 0  TMA producer: A tile [128 rows x 64 k] and B tile [256 n x 64 k]
 //           per stage, 128-byte swizzle, 4-stage ring in shared memory.
 //   warp 1  tcgen05.mma issuer (one thread): 128x256x16 bf16 MMAs, fp32
@@ -22,8 +22,11 @@
 //           the fixed tree (one warp per 32 rows x 128 columns = one private
 //           slot).  The rows' grad_out slices are fetched before the
 //           accumulator is ready.
+//   warp 10 tile scheduler: claims tiles, decodes each into (expert, rows,
+//           columns) a few tiles ahead of use and queues the decoded tile
+//           for the other roles, so no role decodes on its critical path.
 // Tiles (one m-tile x one n-tile of one expert) are ordered so that heavy and
-// light experts' work interleaves (see decode_tile) and handed out dynamically
+// light experts' work interleaves (see decode_tile_warp) and handed out dynamically
 // through a global counter: each output element is produced by exactly one
 // tile with a fixed k order, so the result does not depend on which CTA runs
 // it, on the order, or on the grid size.
@@ -49,10 +52,18 @@ constexpr int ACC_BUFS = 2;
 constexpr int TMEM_COLS = ACC_BUFS * BN;  // 512 = all of tensor memory
 constexpr int EPI_WARP0 = 2;
 constexpr int EPI_WARPS = 8;                  // two per TMEM lane quarter
-constexpr int NUM_THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
+constexpr int SCHED_WARP = EPI_WARP0 + EPI_WARPS;
+constexpr int NUM_THREADS = 32 * (SCHED_WARP + 1);
 constexpr int SLOT = DMOE_SLOT_COLS;
-constexpr int TQ = 4;                         // tile-queue depth (producer runs <= 3 tiles ahead)
+constexpr int TQ = 4;                         // tile-queue depth (the scheduler runs <= 3 tiles ahead)
 constexpr int HEAVY_MT = 3;                   // experts with >= 3 m-tiles reuse each weight slice 3+ times
+
+// A decoded tile as the scheduler queues it: cur = tile index (-1 = no more
+// tiles), e = expert, rows [row0, row_end) of that expert's range starting at
+// row0 (the tile covers row0 .. row0 + BM - 1), columns n0 .. n0 + BN - 1.
+struct QTile {
+  int cur, e, row0, row_end, n0, pad0, pad1, pad2;
+};
 
 struct alignas(8) Ctrl {
   uint64_t full[STAGES];
@@ -60,9 +71,9 @@ struct alignas(8) Ctrl {
   uint64_t acc_full[ACC_BUFS];
   uint64_t acc_empty[ACC_BUFS];
   uint64_t mma_done;
-  uint64_t tq_full[TQ];                  // tile queue: producer -> MMA + epilogue
-  uint64_t tq_empty[TQ];                 // slot consumed by the MMA thread and all epilogue warps
-  int tq_tile[TQ];                       // tile index, -1 = no more tiles
+  uint64_t tq_full[TQ];                  // tile queue: scheduler -> producer, MMA and epilogue
+  uint64_t tq_empty[TQ];                 // slot consumed by the producer, the MMA thread and all epilogue warps
+  QTile tq[TQ];
   uint32_t tmem_base;
   int abort;
   int bad;
@@ -73,6 +84,7 @@ struct alignas(8) Ctrl {
 
 constexpr int STG_BYTES = 32 * 64;             // per epilogue warp: 32 rows x 32 bf16
 constexpr size_t kSmemBytes = 1024 + size_t(STAGES) * STAGE_BYTES + size_t(EPI_WARPS) * STG_BYTES + sizeof(Ctrl);
+static_assert(kSmemBytes <= 232448, "dynamic shared memory above the 227 KB a CTA may use");
 
 struct KParams {
   const int32_t* offsets;
@@ -109,10 +121,6 @@ constexpr uint32_t kIdesc = (1u << 4)                       // D format: f32
                             | (uint32_t(BN >> 3) << 17)     // N >> 3
                             | (uint32_t(BM >> 4) << 24);    // M >> 4
 
-struct Tile {
-  int e, row0, row_end, n0;
-};
-
 // Tile order.  A unit is one m-tile of one expert; its NT n-tiles are
 // consecutive tiles (they share the X rows in L2).  Units of heavy experts
 // (compute-bound: each weight slice serves >= HEAVY_MT m-tiles) and of light
@@ -121,25 +129,35 @@ struct Tile {
 // so both the tensor cores and HBM stay busy; within each class units follow
 // expert order, so an expert's weight slices are reused while resident.
 // The order only decides when a tile runs, never what it computes.
-__device__ __forceinline__ Tile decode_tile(int t, const Ctrl& c, int E, int NT, int H, int U) {
+//
+// Decoded by the whole scheduler warp (called with all 32 lanes): the expert
+// is the largest e < E with pre[e] <= u in the class's exclusive m-tile
+// prefix, found with two ballots (every 32nd entry, then the 32 entries of
+// that segment; E <= 1024) instead of a serial binary search.
+__device__ __forceinline__ QTile decode_tile_warp(int t, const Ctrl& c, int E, int NT, int H, int U, int lane) {
   const int p = t / NT;
   const int n_tile = t - p * NT;
   const int i = int((long long)p * H / U);                   // heavy units before position p
   const bool heavy = (long long)(p + 1) * H / U > i;
   const int* pre = heavy ? c.hp : c.cp;
   const int u = heavy ? i : p - i;
-  // largest e in [0, E) with pre[e] <= u (skips experts of the other class and empty ones)
-  int lo = 0, hi = E;
-  while (hi - lo > 1) {
-    int mid = (lo + hi) >> 1;
-    if (pre[mid] <= u) lo = mid; else hi = mid;
-  }
-  Tile tl;
-  tl.e = lo;
-  tl.row0 = c.off[lo] + (u - pre[lo]) * BM;
-  tl.row_end = c.off[lo + 1];
-  tl.n0 = n_tile * BN;
-  return tl;
+  const int e1 = lane * 32;
+  const unsigned m1 = __ballot_sync(0xffffffffu, e1 < E && pre[e1] <= u);   // lane 0 always (pre[0] = 0)
+  const int seg = 31 - __clz(m1);
+  const int e2 = seg * 32 + lane;
+  const int v2 = e2 < E ? pre[e2] : 0x7fffffff;
+  const unsigned m2 = __ballot_sync(0xffffffffu, v2 <= u);
+  const int l2 = 31 - __clz(m2);
+  const int e = seg * 32 + l2;
+  const int pe = __shfl_sync(0xffffffffu, v2, l2);
+  QTile q;
+  q.cur = t;
+  q.e = e;
+  q.row0 = c.off[e] + (u - pe) * BM;
+  q.row_end = c.off[e + 1];
+  q.n0 = n_tile * BN;
+  q.pad0 = q.pad1 = q.pad2 = 0;
+  return q;
 }
 
 template <int MODE>
@@ -168,7 +186,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
     mbar_init(smem_u32(&c.mma_done), 1);
     for (int i = 0; i < TQ; ++i) {
       mbar_init(smem_u32(&c.tq_full[i]), 1);
-      mbar_init(smem_u32(&c.tq_empty[i]), 1 + EPI_WARPS);
+      mbar_init(smem_u32(&c.tq_empty[i]), 2 + EPI_WARPS);   // producer, MMA thread, epilogue warps
     }
     c.abort = 0;
     c.bad = 0;
@@ -236,28 +254,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
       bool skipped_first = false;
       int stage = 0;
       uint32_t ph = 0;
-      // Tiles are handed out dynamically (first tile = blockIdx.x, then a
-      // global counter), so neighbouring tiles -- which share weight slices
-      // and X rows in L2 -- run at nearly the same time on different SMs.
-      // Which CTA computes a tile never changes its bits.
-      // The serialized control claims every tile from the counter, so a tile
-      // is owned only by a CTA that is already running: its writers wait on
-      // earlier-claimed tiles only, which always make progress.
-      constexpr bool kClaimAll = MODE == int(GemmMode::kSerial);
-      int tile = kClaimAll ? atomicAdd(p.sched, 1) : int(blockIdx.x);
       for (int qi = 0;; ++qi) {
         const int qs = qi % TQ;
-        if (!mbar_wait(smem_u32(&c.tq_empty[qs]), uint32_t((qi / TQ) & 1) ^ 1u, &c.abort, p.status, p.wait_ns)) break;
-        // the serialized control claims n-tile-major (every m-tile's n-tile 0,
-        // then every n-tile 1, ...), so a writer's predecessor was claimed a
-        // whole round earlier; queued tiles carry the usual unit-major index
-        const int cur = tile >= total_tiles ? -1
-                        : kClaimAll ? (tile % units) * p.NT + tile / units : tile;
-        c.tq_tile[qs] = cur;
-        mbar_arrive(smem_u32(&c.tq_full[qs]));
-        if (cur < 0) break;
-        tile = (kClaimAll ? 0 : int(gridDim.x)) + atomicAdd(p.sched, 1);   // fetched early: latency hides behind the loads
-        const Tile tl = decode_tile(cur, c, E, p.NT, units_heavy, units);
+        if (!mbar_wait(smem_u32(&c.tq_full[qs]), uint32_t((qi / TQ) & 1), &c.abort, p.status, p.wait_ns)) break;
+        const QTile tl = c.tq[qs];
+        mbar_arrive(smem_u32(&c.tq_empty[qs]));
+        if (tl.cur < 0) break;
         const int brow = tl.e * p.N + tl.n0;
         bool ok = true;
         for (int kb = 0; kb < p.KB; ++kb) {
@@ -295,7 +297,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
       for (int qi = 0;; ++qi) {
         const int qs = qi % TQ;
         if (!mbar_wait(smem_u32(&c.tq_full[qs]), uint32_t((qi / TQ) & 1), &c.abort, p.status, p.wait_ns)) break;
-        const int cur = c.tq_tile[qs];
+        const int cur = c.tq[qs].cur;
         mbar_arrive(smem_u32(&c.tq_empty[qs]));
         if (cur < 0) break;
         if (!mbar_wait(smem_u32(&c.acc_empty[acc]), aph ^ 1u, &c.abort, p.status, p.wait_ns)) break;
@@ -325,6 +327,44 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
       tc_commit(smem_u32(&c.mma_done));
       mbar_wait_drain(smem_u32(&c.mma_done), 0, p.wait_ns / 4);
     }
+  } else if (warp == SCHED_WARP) {
+    // -------------------------------------------------- tile scheduler (one warp)
+    // Tiles are handed out dynamically (first tile = blockIdx.x, then a
+    // global counter), so neighbouring tiles -- which share weight slices
+    // and X rows in L2 -- run at nearly the same time on different SMs.
+    // Which CTA computes a tile never changes its bits.  Each claimed tile
+    // is decoded while its queue slot is still in use and queued as soon as
+    // the slot frees, so the producer moves from one tile's last stage to
+    // the next tile's first without a pause; the next claim is in flight
+    // meanwhile.
+    // The serialized control claims every tile from the counter, so a tile
+    // is owned only by a CTA that is already running: its writers wait on
+    // earlier-claimed tiles only, which always make progress.
+    constexpr bool kClaimAll = MODE == int(GemmMode::kSerial);
+    int tile = 0;
+    if (lane == 0) tile = kClaimAll ? atomicAdd(p.sched, 1) : int(blockIdx.x);
+    tile = __shfl_sync(0xffffffffu, tile, 0);
+    for (int qi = 0;; ++qi) {
+      const int qs = qi % TQ;
+      // the serialized control claims n-tile-major (every m-tile's n-tile 0,
+      // then every n-tile 1, ...), so a writer's predecessor was claimed a
+      // whole round earlier; queued tiles carry the usual unit-major index
+      const int cur = tile >= total_tiles ? -1
+                      : kClaimAll ? (tile % units) * p.NT + tile / units : tile;
+      int nxt = 0;
+      if (cur >= 0 && lane == 0) nxt = (kClaimAll ? 0 : int(gridDim.x)) + atomicAdd(p.sched, 1);
+      QTile q{};
+      q.cur = -1;
+      if (cur >= 0) q = decode_tile_warp(cur, c, E, p.NT, units_heavy, units, lane);
+      if (!warp_wait(smem_u32(&c.tq_empty[qs]), uint32_t((qi / TQ) & 1) ^ 1u, &c.abort, p.status, lane, p.wait_ns))
+        break;
+      if (lane == 0) {
+        c.tq[qs] = q;
+        mbar_arrive(smem_u32(&c.tq_full[qs]));
+      }
+      if (cur < 0) break;
+      tile = __shfl_sync(0xffffffffu, nxt, 0);
+    }
   } else {
     // -------------------------------------------------- epilogue (8 warps)
     // Warp w may only read TMEM lanes 32*(w%4)..+31; warps 2-5 take the first
@@ -345,11 +385,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
     for (int qi = 0;; ++qi) {
       const int qs = qi % TQ;
       if (!warp_wait(smem_u32(&c.tq_full[qs]), uint32_t((qi / TQ) & 1), &c.abort, p.status, lane, p.wait_ns)) break;
-      const int cur = c.tq_tile[qs];
+      const QTile tl = c.tq[qs];
+      const int cur = tl.cur;
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&c.tq_empty[qs]));
       if (cur < 0) break;
-      const Tile tl = decode_tile(cur, c, E, p.NT, units_heavy, units);
       const int col0 = tl.n0 + h * SLOT;
       const bool active = col0 < p.N;           // warp-uniform: a half-width last N-tile
       // rows of this lane in the coalesced layout: q*32 + i*8 + lane/4, i = 0..3
@@ -491,8 +531,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
     tmem_dealloc(tmem_base, TMEM_COLS);
   }
   if (tid == 0) {
-    // this thread made the CTA's last counter fetch; the last CTA to finish
-    // zeroes both counters for the next launch on this stream
+    // every counter fetch of this CTA (made by its scheduler warp) has
+    // returned before the barrier above; the last CTA to finish zeroes both
+    // counters for the next launch on this stream
     __threadfence();
     if (atomicAdd(p.sched + 1, 1) == int(gridDim.x) - 1) {
       atomicExch(p.sched, 0);

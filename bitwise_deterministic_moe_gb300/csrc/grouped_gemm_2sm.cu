@@ -18,13 +18,15 @@
 // stage barrier; the leader's MMA commits free the stage in both CTAs
 // (multicast) and publish finished accumulators to both epilogues.
 //
-// Roles per CTA (320 threads): warp 0 TMA producer; warp 1 tensor-memory
+// Roles per CTA (352 threads): warp 0 TMA producer; warp 1 tensor-memory
 // owner and, in the leader, the single MMA-issuing thread (in the other CTA,
 // a forwarder that turns its epilogue's local releases into one
 // cluster-scope arrival each); warps 2-9 the epilogue (identical to the
-// single-CTA kernel, on this CTA's 128 rows).
-// The leader's producer takes tiles from the global counter and forwards each
-// tile index to the other CTA through distributed shared memory.
+// single-CTA kernel, on this CTA's 128 rows); warp 10, in the leader only,
+// the tile scheduler: it takes tiles from the global counter, decodes each
+// into (expert, rows, columns) a few tiles ahead of use and queues the
+// decoded tile in both CTAs (the other CTA's copy through distributed shared
+// memory), so no role decodes on its critical path.
 // Every wait is bounded; a timeout in either CTA aborts both.
 #include <cuda.h>
 
@@ -52,23 +54,32 @@ constexpr int ACC_BUFS = 2;
 constexpr int TMEM_COLS = ACC_BUFS * BN;
 constexpr int EPI_WARP0 = 2;
 constexpr int EPI_WARPS = 8;
-constexpr int NUM_THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
+constexpr int SCHED_WARP = EPI_WARP0 + EPI_WARPS;
+constexpr int NUM_THREADS = 32 * (SCHED_WARP + 1);
 constexpr int SLOT = DMOE_SLOT_COLS;
 constexpr int TQ = 4;
 constexpr int HEAVY_MT = 2;              // pair m-tiles (256 rows) per expert that make it compute-bound
 constexpr int STG_BYTES = 32 * 64;
 
-struct alignas(8) Ctrl {
+// A decoded tile as the scheduler queues it: cur = tile index (-1 = no more
+// tiles), e = expert, row0 = first row of the PAIR tile (the tile covers
+// row0 .. row0 + PM - 1), row_end = end of the expert's rows, columns
+// n0 .. n0 + BN - 1.
+struct alignas(16) QTile {
+  int cur, e, row0, row_end, n0, pad0, pad1, pad2;
+};
+
+struct alignas(16) Ctrl {
   uint64_t full[STAGES];                 // leader: both CTAs' halves of a stage landed
   uint64_t empty[STAGES];                // each CTA: the pair's MMAs are done with the stage
   uint64_t acc_full[ACC_BUFS];           // each CTA: accumulator ready
   uint64_t acc_empty[ACC_BUFS];          // leader: both CTAs' epilogues drained the accumulator
   uint64_t mma_done;
-  uint64_t tq_full[TQ];                  // each CTA: tile index published by the leader
+  uint64_t tq_full[TQ];                  // each CTA: decoded tile published by the leader's scheduler
   uint64_t tq_empty[TQ];                 // leader: every consumer of both CTAs read the slot
   uint64_t tq_read[TQ];                  // other CTA: its epilogue warps read the slot
   uint64_t acc_read[ACC_BUFS];           // other CTA: its epilogue warps drained the accumulator
-  int tq_tile[TQ];
+  QTile tq[TQ];
   uint32_t tmem_base;
   int abort;
   int off[DMOE_MAX_EXPERTS + 1];
@@ -78,6 +89,7 @@ struct alignas(8) Ctrl {
 
 constexpr size_t kSmemBytes =
     1024 + size_t(STAGES) * STAGE_BYTES + size_t(EPI_WARPS) * STG_BYTES + sizeof(Ctrl);
+static_assert(kSmemBytes <= 232448, "dynamic shared memory above the 227 KB a CTA may use");
 
 struct KParams {
   const int32_t* offsets;
@@ -108,29 +120,32 @@ __device__ __forceinline__ uint64_t smem_desc_k128(uint32_t saddr) {
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(BN >> 3) << 17) |
                             (uint32_t(PM >> 4) << 24);
 
-struct Tile {
-  int e, row0, row_end, n0;   // row0 = first row of the PAIR tile
-};
-
-// Same order as the single-CTA kernel, in units of one 256-row pair m-tile.
-__device__ __forceinline__ Tile decode_tile(int t, const Ctrl& c, int E, int NT, int H, int U) {
+// Same order as the single-CTA kernel, in units of one 256-row pair m-tile;
+// decoded by the whole scheduler warp with two ballots (E <= 1024).
+__device__ __forceinline__ QTile decode_tile_warp(int t, const Ctrl& c, int E, int NT, int H, int U, int lane) {
   const int p = t / NT;
   const int n_tile = t - p * NT;
   const int i = int((long long)p * H / U);
   const bool heavy = (long long)(p + 1) * H / U > i;
   const int* pre = heavy ? c.hp : c.cp;
   const int u = heavy ? i : p - i;
-  int lo = 0, hi = E;
-  while (hi - lo > 1) {
-    int mid = (lo + hi) >> 1;
-    if (pre[mid] <= u) lo = mid; else hi = mid;
-  }
-  Tile tl;
-  tl.e = lo;
-  tl.row0 = c.off[lo] + (u - pre[lo]) * PM;
-  tl.row_end = c.off[lo + 1];
-  tl.n0 = n_tile * BN;
-  return tl;
+  const int e1 = lane * 32;
+  const unsigned m1 = __ballot_sync(0xffffffffu, e1 < E && pre[e1] <= u);   // lane 0 always (pre[0] = 0)
+  const int seg = 31 - __clz(m1);
+  const int e2 = seg * 32 + lane;
+  const int v2 = e2 < E ? pre[e2] : 0x7fffffff;
+  const unsigned m2 = __ballot_sync(0xffffffffu, v2 <= u);
+  const int l2 = 31 - __clz(m2);
+  const int e = seg * 32 + l2;
+  const int pe = __shfl_sync(0xffffffffu, v2, l2);
+  QTile q;
+  q.cur = t;
+  q.e = e;
+  q.row0 = c.off[e] + (u - pe) * PM;
+  q.row_end = c.off[e + 1];
+  q.n0 = n_tile * BN;
+  q.pad0 = q.pad1 = q.pad2 = 0;
+  return q;
 }
 
 // Bounded wait that also raises the other CTA's abort flag when it gives up.
@@ -189,8 +204,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
     mbar_init(smem_u32(&c.mma_done), 1);
     for (int i = 0; i < TQ; ++i) {
       mbar_init(smem_u32(&c.tq_full[i]), 1);
-      // leader: its MMA thread + its epilogue warps + the other CTA's producer and forwarder
-      mbar_init(smem_u32(&c.tq_empty[i]), 1 + EPI_WARPS + 2);
+      // leader: its producer, MMA thread and epilogue warps + the other CTA's producer and forwarder
+      mbar_init(smem_u32(&c.tq_empty[i]), 2 + EPI_WARPS + 2);
       mbar_init(smem_u32(&c.tq_read[i]), EPI_WARPS);
     }
     c.abort = 0;
@@ -256,40 +271,13 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
       uint32_t ph = 0;
       bool in_flight = false;
       int armed_total = 0;         // leader: stages armed so far (round-robin over STAGES)
-      int tile = pair_id;          // leader: next tile to publish
-      int published = 0;           // leader: queue positions published so far
-      bool done_publishing = false;
-      bool aborted = false;
       for (int qi = 0;; ++qi) {
         const int qs = qi % TQ;
-        int cur;
-        if (leader) {
-          // Publish one tile ahead of this thread's own loads, so the other
-          // CTA starts loading a tile as early as the leader does.
-          while (!done_publishing && published <= qi + 1) {
-            const int ps = published % TQ;
-            if (!pwait<true>(smem_u32(&c.tq_empty[ps]), uint32_t((published / TQ) & 1) ^ 1u, c, p, peer_abort)) {
-              aborted = true;
-              break;
-            }
-            const int t = tile < total_tiles ? tile : -1;
-            c.tq_tile[ps] = t;
-            st_cluster_s32(mapa_shared(smem_u32(&c.tq_tile[ps]), peer), t);
-            mbar_arrive(smem_u32(&c.tq_full[ps]));
-            mbar_arrive_cluster(mapa_shared(smem_u32(&c.tq_full[ps]), peer));
-            ++published;
-            if (t >= 0) tile = n_pairs + atomicAdd(p.sched, 1);
-            else done_publishing = true;
-          }
-          if (aborted || published <= qi) break;
-          cur = c.tq_tile[qs];     // written by this thread; not reused before position qi + TQ
-        } else {
-          if (!pwait<true>(smem_u32(&c.tq_full[qs]), uint32_t((qi / TQ) & 1), c, p, peer_abort)) break;
-          cur = c.tq_tile[qs];
-          mbar_arrive_cluster(mapa_shared(smem_u32(&c.tq_empty[qs]), peer));
-        }
-        if (cur < 0) break;
-        const Tile tl = decode_tile(cur, c, E, p.NT, units_heavy, units);
+        if (!pwait<true>(smem_u32(&c.tq_full[qs]), uint32_t((qi / TQ) & 1), c, p, peer_abort)) break;
+        const QTile tl = c.tq[qs];
+        if (leader) mbar_arrive(smem_u32(&c.tq_empty[qs]));
+        else mbar_arrive_cluster(mapa_shared(smem_u32(&c.tq_empty[qs]), peer));
+        if (tl.cur < 0) break;
         const int arow = tl.row0 + int(rank) * BM;
         const int brow = tl.e * p.N + tl.n0 + int(rank) * BNH;
         bool ok = true;
@@ -341,7 +329,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
         const int qs = qi % TQ;
         const uint32_t qph = uint32_t((qi / TQ) & 1);
         if (!pwait<true>(smem_u32(&c.tq_full[qs]), qph, c, p, peer_abort)) break;
-        const int cur = c.tq_tile[qs];
+        const int cur = c.tq[qs].cur;
         if (!pwait<false>(smem_u32(&c.tq_read[qs]), qph, c, p, peer_abort)) break;
         mbar_arrive_cluster(mapa_shared(smem_u32(&c.tq_empty[qs]), peer));
         if (cur < 0) break;
@@ -359,7 +347,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
       for (int qi = 0;; ++qi) {
         const int qs = qi % TQ;
         if (!pwait<false>(smem_u32(&c.tq_full[qs]), uint32_t((qi / TQ) & 1), c, p, peer_abort)) break;
-        const int cur = c.tq_tile[qs];
+        const int cur = c.tq[qs].cur;
         mbar_arrive(smem_u32(&c.tq_empty[qs]));
         if (cur < 0) break;
         if (!pwait<true>(smem_u32(&c.acc_empty[acc]), aph ^ 1u, c, p, peer_abort)) break;
@@ -386,6 +374,43 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
       tc_commit_pair(smem_u32(&c.mma_done));
       mbar_wait_drain(smem_u32(&c.mma_done), 0, p.wait_ns / 4);
     }
+  } else if (warp == SCHED_WARP) {
+    if (leader) {
+      // ------------------------------------------------ tile scheduler (leader, one warp)
+      // First tile = the pair index, then the global counter.  Each claimed
+      // tile is decoded while its queue slot is still in use and published
+      // to both CTAs as soon as every consumer of both has released the
+      // slot; the next claim is in flight meanwhile.
+      int tile = 0;
+      if (lane == 0) tile = pair_id;
+      tile = __shfl_sync(0xffffffffu, tile, 0);
+      for (int qi = 0;; ++qi) {
+        const int qs = qi % TQ;
+        const int cur = tile < total_tiles ? tile : -1;
+        int nxt = 0;
+        if (cur >= 0 && lane == 0) nxt = n_pairs + atomicAdd(p.sched, 1);
+        QTile q{};
+        q.cur = -1;
+        if (cur >= 0) q = decode_tile_warp(cur, c, E, p.NT, units_heavy, units, lane);
+        if (!pwarp_wait<true>(smem_u32(&c.tq_empty[qs]), uint32_t((qi / TQ) & 1) ^ 1u, c, p, peer_abort, lane))
+          break;
+        if (lane == 0) {
+          c.tq[qs] = q;
+          // the other CTA's copy: eight words through distributed shared
+          // memory, made visible by the release of the arrival that follows
+          const uint32_t dst = mapa_shared(smem_u32(&c.tq[qs]), peer);
+          st_cluster_s32(dst + 0, q.cur);
+          st_cluster_s32(dst + 4, q.e);
+          st_cluster_s32(dst + 8, q.row0);
+          st_cluster_s32(dst + 12, q.row_end);
+          st_cluster_s32(dst + 16, q.n0);
+          mbar_arrive(smem_u32(&c.tq_full[qs]));
+          mbar_arrive_cluster(mapa_shared(smem_u32(&c.tq_full[qs]), peer));
+        }
+        if (cur < 0) break;
+        tile = __shfl_sync(0xffffffffu, nxt, 0);
+      }
+    }
   } else {
     // -------------------------------------------------- epilogue (8 warps, both CTAs)
     const int q = warp & 3;
@@ -398,13 +423,13 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
     for (int qi = 0;; ++qi) {
       const int qs = qi % TQ;
       if (!pwarp_wait<true>(smem_u32(&c.tq_full[qs]), uint32_t((qi / TQ) & 1), c, p, peer_abort, lane)) break;
-      const int cur = c.tq_tile[qs];
+      const QTile tl = c.tq[qs];
+      const int cur = tl.cur;
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(smem_u32(leader ? &c.tq_empty[qs] : &c.tq_read[qs]));
       }
       if (cur < 0) break;
-      const Tile tl = decode_tile(cur, c, E, p.NT, units_heavy, units);
       const int col0 = tl.n0 + h * SLOT;
       const bool active = col0 < p.N;
       const int row_cta = tl.row0 + int(rank) * BM;
