@@ -13,8 +13,10 @@
 // own shared memory, and receives its 128 rows of the fp32 accumulator in its
 // own tensor memory.  Per SM and per MMA cycle this halves the B operand that
 // shared memory must supply and that TMA must bring in, which is what limits
-// a single-CTA 128x256 tile on this part, and a stage shrinks to 32 KB so six
-// fit.  Both CTAs load their halves with TMA and signal the leader's
+// a single-CTA 128x256 tile on this part, and a stage shrinks to 32 KB so
+// seven fit: the kernel keeps nothing else in shared memory (the expert
+// tables live in the scheduler warp's registers, and the epilogue transposes
+// through warp shuffles instead of a staging buffer).  Both CTAs load their halves with TMA and signal the leader's
 // stage barrier; the leader's MMA commits free the stage in both CTAs
 // (multicast) and publish finished accumulators to both epilogues.
 //
@@ -36,7 +38,6 @@
 namespace dmoe {
 
 bool make_tmap_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows);
-bool make_tmap_bf16_store32(CUtensorMap* m, void* ptr, uint64_t rows, uint64_t cols);
 
 namespace {
 
@@ -46,7 +47,7 @@ constexpr int BN = 256;                  // columns per tile (UMMA N)
 constexpr int BNH = BN / 2;              // B rows held by each CTA
 constexpr int BK = 64;                   // k per stage: one 128-byte swizzle row of bf16
 constexpr int UMMA_K = 16;
-constexpr int STAGES = 6;
+constexpr int STAGES = 7;
 constexpr int A_STAGE_BYTES = BM * BK * 2;     // 16 KB
 constexpr int B_STAGE_BYTES = BNH * BK * 2;    // 16 KB
 constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
@@ -59,7 +60,6 @@ constexpr int NUM_THREADS = 32 * (SCHED_WARP + 1);
 constexpr int SLOT = DMOE_SLOT_COLS;
 constexpr int TQ = 4;
 constexpr int HEAVY_MT = 2;              // pair m-tiles (256 rows) per expert that make it compute-bound
-constexpr int STG_BYTES = 32 * 64;
 
 // A decoded tile as the scheduler queues it: cur = tile index (-1 = no more
 // tiles), e = expert, row0 = first row of the PAIR tile (the tile covers
@@ -82,13 +82,9 @@ struct alignas(16) Ctrl {
   QTile tq[TQ];
   uint32_t tmem_base;
   int abort;
-  int off[DMOE_MAX_EXPERTS + 1];
-  int hp[DMOE_MAX_EXPERTS + 1];
-  int cp[DMOE_MAX_EXPERTS + 1];
 };
 
-constexpr size_t kSmemBytes =
-    1024 + size_t(STAGES) * STAGE_BYTES + size_t(EPI_WARPS) * STG_BYTES + sizeof(Ctrl);
+constexpr size_t kSmemBytes = 1024 + size_t(STAGES) * STAGE_BYTES + sizeof(Ctrl);
 static_assert(kSmemBytes <= 232448, "dynamic shared memory above the 227 KB a CTA may use");
 
 struct KParams {
@@ -120,32 +116,143 @@ __device__ __forceinline__ uint64_t smem_desc_k128(uint32_t saddr) {
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(BN >> 3) << 17) |
                             (uint32_t(PM >> 4) << 24);
 
-// Same order as the single-CTA kernel, in units of one 256-row pair m-tile;
-// decoded by the whole scheduler warp with two ballots (E <= 1024).
-__device__ __forceinline__ QTile decode_tile_warp(int t, const Ctrl& c, int E, int NT, int H, int U, int lane) {
+// The scheduler warp's expert tables, held in registers: lane l holds experts
+// e = 32 l + j (j = 0..31; E <= 1024), with off[e .. e + 32] (o), and the
+// exclusive prefixes of the pair m-tiles of heavy (hp) and light (cp)
+// experts before e.  All indices are compile-time after unrolling, so the
+// arrays stay in registers.
+struct ExpertTables {
+  int o[33];
+  int hp[32];
+  int cp[32];
+};
+
+// Loads the offsets, validates them (non-decreasing, off[0] = 0, off[E] = R)
+// and builds the prefixes; returns the units of each class through hu / lu
+// and whether the offsets are bad (warp-uniform).
+__device__ __forceinline__ bool build_tables(ExpertTables& t, const int32_t* offsets, int E, int R, int lane,
+                                             int& hu, int& lu) {
+  bool bad = false;
+#pragma unroll
+  for (int j = 0; j <= 32; ++j) {
+    const int e = 32 * lane + j;
+    t.o[j] = e <= E ? offsets[e] : 0;
+    if (e == E && t.o[j] != R) bad = true;
+  }
+  if (lane == 0 && t.o[0] != 0) bad = true;
+  int hsum = 0, csum = 0;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const int e = 32 * lane + j;
+    int mt = 0;
+    if (e < E) {
+      if (t.o[j + 1] < t.o[j]) bad = true;
+      mt = t.o[j + 1] > t.o[j] ? (t.o[j + 1] - t.o[j] + PM - 1) / PM : 0;
+    }
+    t.hp[j] = hsum;
+    t.cp[j] = csum;
+    hsum += mt >= HEAVY_MT ? mt : 0;
+    csum += mt >= HEAVY_MT ? 0 : mt;
+  }
+  int hx = hsum, cx = csum;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int hv = __shfl_up_sync(0xffffffffu, hx, d);
+    const int cv = __shfl_up_sync(0xffffffffu, cx, d);
+    if (lane >= d) {
+      hx += hv;
+      cx += cv;
+    }
+  }
+  hu = __shfl_sync(0xffffffffu, hx, 31);
+  lu = __shfl_sync(0xffffffffu, cx, 31);
+  hx -= hsum;
+  cx -= csum;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    t.hp[j] += hx;
+    t.cp[j] += cx;
+  }
+  return __any_sync(0xffffffffu, bad);
+}
+
+// Same order as the single-CTA kernel, in units of one 256-row pair m-tile,
+// decoded by the whole scheduler warp from its register tables: the expert
+// is the largest e < E whose class prefix is <= u; the lanes whose first
+// expert qualifies form a prefix of the warp, the last of them holds e, and
+// within it the qualifying experts are a prefix of its 32.
+__device__ __forceinline__ QTile decode_tile_warp(int t, const ExpertTables& tb, int E, int NT, int H, int U,
+                                                  int lane) {
   const int p = t / NT;
   const int n_tile = t - p * NT;
   const int i = int((long long)p * H / U);
   const bool heavy = (long long)(p + 1) * H / U > i;
-  const int* pre = heavy ? c.hp : c.cp;
   const int u = heavy ? i : p - i;
-  const int e1 = lane * 32;
-  const unsigned m1 = __ballot_sync(0xffffffffu, e1 < E && pre[e1] <= u);   // lane 0 always (pre[0] = 0)
-  const int seg = 31 - __clz(m1);
-  const int e2 = seg * 32 + lane;
-  const int v2 = e2 < E ? pre[e2] : 0x7fffffff;
-  const unsigned m2 = __ballot_sync(0xffffffffu, v2 <= u);
-  const int l2 = 31 - __clz(m2);
-  const int e = seg * 32 + l2;
-  const int pe = __shfl_sync(0xffffffffu, v2, l2);
+  // the class's prefix selected with a mask, element by element, so that the
+  // tables are never addressed through a pointer (they must stay in registers)
+  const int hm = heavy ? -1 : 0;
+  int cnt = 0;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const int pv = (tb.hp[j] & hm) | (tb.cp[j] & ~hm);
+    cnt += (32 * lane + j < E && pv <= u) ? 1 : 0;
+  }
+  const int seg = 31 - __clz(__ballot_sync(0xffffffffu, cnt > 0));   // lane 0 always (prefix 0 <= u)
+  int pe = 0, oe = 0, oe1 = 0;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const int hj = j == cnt - 1 ? -1 : 0;
+    pe = (((tb.hp[j] & hm) | (tb.cp[j] & ~hm)) & hj) | (pe & ~hj);
+    oe = (tb.o[j] & hj) | (oe & ~hj);
+    oe1 = (tb.o[j + 1] & hj) | (oe1 & ~hj);
+  }
+  const int c = __shfl_sync(0xffffffffu, cnt, seg);
+  pe = __shfl_sync(0xffffffffu, pe, seg);
+  oe = __shfl_sync(0xffffffffu, oe, seg);
+  oe1 = __shfl_sync(0xffffffffu, oe1, seg);
   QTile q;
   q.cur = t;
-  q.e = e;
-  q.row0 = c.off[e] + (u - pe) * PM;
-  q.row_end = c.off[e + 1];
+  q.e = 32 * seg + c - 1;
+  q.row0 = oe + (u - pe) * PM;
+  q.row_end = oe1;
   q.n0 = n_tile * BN;
   q.pad0 = q.pad1 = q.pad2 = 0;
   return q;
+}
+
+__device__ __forceinline__ uint4 shfl_xor_u4(const uint4& v, int m) {
+  uint4 r;
+  r.x = __shfl_xor_sync(0xffffffffu, v.x, m);
+  r.y = __shfl_xor_sync(0xffffffffu, v.y, m);
+  r.z = __shfl_xor_sync(0xffffffffu, v.z, m);
+  r.w = __shfl_xor_sync(0xffffffffu, v.w, m);
+  return r;
+}
+
+// 4 x 4 transpose of 16-byte pieces inside each quad of lanes: lane 4a + b
+// enters with pieces 0..3 of its own row and leaves with piece b of rows
+// 4a + 0 .. 4a + 3 (two exchange rounds, across lane bits 0 and 1).
+// Lane-dependent choices are made with masks, element by element, so the
+// pieces are never addressed through an index (they must stay in registers).
+__device__ __forceinline__ uint4 mask_sel(uint32_t m, const uint4& a, const uint4& b) {   // m ? a : b
+  return make_uint4((a.x & m) | (b.x & ~m), (a.y & m) | (b.y & ~m), (a.z & m) | (b.z & ~m), (a.w & m) | (b.w & ~m));
+}
+
+__device__ __forceinline__ void quad_transpose(uint4 (&x)[4], int lane) {
+  const uint32_t odd = (lane & 1) ? 0xffffffffu : 0u;
+#pragma unroll
+  for (int j = 0; j < 4; j += 2) {
+    const uint4 r = shfl_xor_u4(mask_sel(odd, x[j], x[j + 1]), 1);
+    x[j] = mask_sel(odd, r, x[j]);
+    x[j + 1] = mask_sel(odd, x[j + 1], r);
+  }
+  const uint32_t hi = (lane & 2) ? 0xffffffffu : 0u;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const uint4 r = shfl_xor_u4(mask_sel(hi, x[j], x[j + 2]), 2);
+    x[j] = mask_sel(hi, r, x[j]);
+    x[j + 2] = mask_sel(hi, x[j + 2], r);
+  }
 }
 
 // Bounded wait that also raises the other CTA's abort flag when it gives up.
@@ -176,10 +283,10 @@ __device__ __forceinline__ bool pwarp_wait(uint32_t bar, uint32_t parity, Ctrl& 
 template <int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                         const __grid_constant__ CUtensorMap tmap_o, const KParams p) {
+                         const KParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Ctrl& c = *reinterpret_cast<Ctrl*>(base + size_t(STAGES) * STAGE_BYTES + size_t(EPI_WARPS) * STG_BYTES);
+  Ctrl& c = *reinterpret_cast<Ctrl*>(base + size_t(STAGES) * STAGE_BYTES);
   const uint32_t stage0 = smem_u32(base);
 
   const int tid = threadIdx.x;
@@ -221,45 +328,10 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
     tc_fence_before();
   }
   pdl_begin();   // no global memory is touched above this line
-  for (int e = tid; e <= E; e += NUM_THREADS) c.off[e] = p.offsets[e];
-  __syncthreads();
-  int bad = 0;
-  for (int e = tid; e < E; e += NUM_THREADS) {
-    int a = c.off[e], b = c.off[e + 1];
-    if (b < a) bad = 1;
-    const int mt = (b > a) ? (b - a + PM - 1) / PM : 0;
-    c.hp[e + 1] = mt >= HEAVY_MT ? mt : 0;
-    c.cp[e + 1] = mt >= HEAVY_MT ? 0 : mt;
-  }
-  if (tid == 0) {
-    if (c.off[0] != 0 || c.off[E] != p.R) bad = 1;
-    c.hp[0] = 0;
-    c.cp[0] = 0;
-  }
-  bad = __syncthreads_or(bad);
-  if (warp < 2) {
-    int* pre = warp == 0 ? c.hp : c.cp;
-    int carry = 0;
-    for (int b0 = 1; b0 <= E; b0 += 32) {
-      int i = b0 + lane;
-      int v = (i <= E) ? pre[i] : 0;
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        int u = __shfl_up_sync(0xffffffffu, v, d);
-        if (lane >= d) v += u;
-      }
-      if (i <= E) pre[i] = v + carry;
-      carry += __shfl_sync(0xffffffffu, v, 31);
-    }
-  }
   tc_fence_before();
   // both CTAs' barriers are initialised before either touches the other's
   cluster_sync_all();
   tc_fence_after();
-  if (bad && tid == 0 && leader) record_error(p.status, DMOE_ERR_ROUTING);
-  const int units_heavy = c.hp[E];
-  const int units = c.hp[E] + c.cp[E];
-  const int total_tiles = bad ? 0 : units * p.NT;
   const uint32_t tmem_base = c.tmem_base;
   const int n_pairs = int(gridDim.x) / 2;
   const int pair_id = int(blockIdx.x) / 2;
@@ -381,6 +453,12 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
       // tile is decoded while its queue slot is still in use and published
       // to both CTAs as soon as every consumer of both has released the
       // slot; the next claim is in flight meanwhile.
+      ExpertTables tb;
+      int units_heavy = 0, units_light = 0;
+      const bool bad = build_tables(tb, p.offsets, E, p.R, lane, units_heavy, units_light);
+      if (bad && lane == 0) record_error(p.status, DMOE_ERR_ROUTING);
+      const int units = units_heavy + units_light;
+      const int total_tiles = bad ? 0 : units * p.NT;
       int tile = 0;
       if (lane == 0) tile = pair_id;
       tile = __shfl_sync(0xffffffffu, tile, 0);
@@ -391,7 +469,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
         if (cur >= 0 && lane == 0) nxt = n_pairs + atomicAdd(p.sched, 1);
         QTile q{};
         q.cur = -1;
-        if (cur >= 0) q = decode_tile_warp(cur, c, E, p.NT, units_heavy, units, lane);
+        if (cur >= 0) q = decode_tile_warp(cur, tb, E, p.NT, units_heavy, units, lane);
         if (!pwarp_wait<true>(smem_u32(&c.tq_empty[qs]), uint32_t((qi / TQ) & 1) ^ 1u, c, p, peer_abort, lane))
           break;
         if (lane == 0) {
@@ -416,7 +494,6 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
     const int q = warp & 3;
     const int h = (warp - EPI_WARP0) / 4;
     const int k4 = lane & 3;
-    const uint32_t stg = stage0 + uint32_t(STAGES * STAGE_BYTES + (warp - EPI_WARP0) * STG_BYTES);
     const uint64_t pol_keep = policy_evict_last();
     int acc = 0;
     uint32_t aph = 0;
@@ -433,17 +510,17 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
       const int col0 = tl.n0 + h * SLOT;
       const bool active = col0 < p.N;
       const int row_cta = tl.row0 + int(rank) * BM;
+      // after the quad transpose lane 4a + k4 holds piece k4 of rows 4a + i
+      // (i = 0..3) of this warp's 32: a store instruction covers 64
+      // contiguous bytes of each of eight rows
       int rr[4], src[4];
       bool ok[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        rr[i] = row_cta + q * 32 + i * 8 + (lane >> 2);
+        rr[i] = row_cta + q * 32 + (lane & ~3) + i;
         ok[i] = active && rr[i] < tl.row_end;
         src[i] = 0;
       }
-      // full 32-row quarters leave through TMA tensor stores of the staging
-      // buffer; a ragged quarter at the expert's end stores row by row
-      const bool full32 = active && (row_cta + q * 32 + 32 <= tl.row_end);
       uint4 g[16];
       if (MODE != int(GemmMode::kFwd)) {
 #pragma unroll
@@ -477,36 +554,23 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
           uint32_t v[32];
           tmem_ld_32x32b_x32(tcol + uint32_t(ch * 32), v);
           tmem_wait_ld();
-          if (lane == 0) bulk_wait_group_read<0>();   // the previous chunk's store has read the staging
-          __syncwarp();
+          // row `lane` of the chunk as four 16-byte pieces of bf16
+          uint4 y[4];
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            uint4 y;
-            y.x = pack_bf16x2_rn(__uint_as_float(v[8 * kk + 0]), __uint_as_float(v[8 * kk + 1]));
-            y.y = pack_bf16x2_rn(__uint_as_float(v[8 * kk + 2]), __uint_as_float(v[8 * kk + 3]));
-            y.z = pack_bf16x2_rn(__uint_as_float(v[8 * kk + 4]), __uint_as_float(v[8 * kk + 5]));
-            y.w = pack_bf16x2_rn(__uint_as_float(v[8 * kk + 6]), __uint_as_float(v[8 * kk + 7]));
-            sts_v4(stg + uint32_t(lane * 64 + ((kk ^ ((lane >> 1) & 3)) << 4)), y);
+            y[kk].x = pack_bf16x2_rn(__uint_as_float(v[8 * kk + 0]), __uint_as_float(v[8 * kk + 1]));
+            y[kk].y = pack_bf16x2_rn(__uint_as_float(v[8 * kk + 2]), __uint_as_float(v[8 * kk + 3]));
+            y[kk].z = pack_bf16x2_rn(__uint_as_float(v[8 * kk + 4]), __uint_as_float(v[8 * kk + 5]));
+            y[kk].w = pack_bf16x2_rn(__uint_as_float(v[8 * kk + 6]), __uint_as_float(v[8 * kk + 7]));
           }
-          __syncwarp();
-          if (full32) {
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              tma_store_2d(&tmap_o, stg, col0 + ch * 32, row_cta + q * 32);
-              bulk_commit_group();
-            }
-          }
+          quad_transpose(y, lane);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const int row = i * 8 + (lane >> 2);
-            const uint4 y = lds_v4(stg + uint32_t(row * 64 + ((k4 ^ ((row >> 1) & 3)) << 4)));
             if (ok[i]) {
-              if (!full32) stg_v4(p.out + size_t(rr[i]) * p.N + col0 + ch * 32 + k4 * 8, y);
-              if (MODE != int(GemmMode::kFwd)) slot_accumulate8(a[i], g[ch * 4 + i], y);
+              stg_v4(p.out + size_t(rr[i]) * p.N + col0 + ch * 32 + k4 * 8, y[i]);
+              if (MODE != int(GemmMode::kFwd)) slot_accumulate8(a[i], g[ch * 4 + i], y[i]);
             }
           }
-          __syncwarp();
         }
         if (MODE != int(GemmMode::kFwd)) {
 #pragma unroll
@@ -530,7 +594,6 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
       }
       if (++acc == ACC_BUFS) { acc = 0; aph ^= 1u; }
     }
-    if (lane == 0) bulk_wait_group_all();   // this warp's tensor stores have landed
   }
 
   // No CTA leaves (or frees tensor memory) while the other may still touch
@@ -553,8 +616,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
 }
 
 template <int MODE>
-cudaError_t launch_pair_mode(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to, const KParams& kp,
-                             int grid,
+cudaError_t launch_pair_mode(const CUtensorMap& ta, const CUtensorMap& tb, const KParams& kp, int grid,
                              cudaStream_t stream) {
   const cudaError_t e =
       ensure_kernel_smem(reinterpret_cast<const void*>(grouped_gemm_pair_kernel<MODE>), int(kSmemBytes));
@@ -573,7 +635,7 @@ cudaError_t launch_pair_mode(const CUtensorMap& ta, const CUtensorMap& tb, const
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<MODE>, ta, tb, to, kp);
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<MODE>, ta, tb, kp);
 }
 
 // Largest even CTA count whose pairs can all be resident at once (per device).
@@ -611,8 +673,6 @@ cudaError_t launch_pairs(const GemmArgs& a, cudaStream_t stream) {
   CUtensorMap ta, tb;
   if (!make_tmap_bf16(&ta, a.X, uint64_t(a.R), uint64_t(a.K), BM)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16(&tb, a.W, uint64_t(a.E) * a.N, uint64_t(a.K), BNH)) return cudaErrorInvalidValue;
-  CUtensorMap to;
-  if (!make_tmap_bf16_store32(&to, a.out, uint64_t(a.R), uint64_t(a.N))) return cudaErrorInvalidValue;
   KParams kp;
   kp.offsets = a.offsets;
   kp.E = a.E;
@@ -637,7 +697,7 @@ cudaError_t launch_pairs(const GemmArgs& a, cudaStream_t stream) {
   grid = grid < resident ? grid : resident;    // every pair resident: no pair waits on a queued one
   grid &= ~1;
   if (grid < 2) grid = 2;
-  return launch_pair_mode<MODE>(ta, tb, to, kp, grid, stream);
+  return launch_pair_mode<MODE>(ta, tb, kp, grid, stream);
 }
 
 }  // namespace
