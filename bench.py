@@ -493,7 +493,7 @@ def run_ours(args):
         for a, b in evs:
             if flush:
                 flush_buf.fill_(1)
-                torch.sum(flush_rd, out=flush_sink)
+                torch.sum(flush_rd, dim=0, out=flush_sink)
             a.record(stream)
             fn()
             b.record(stream)
