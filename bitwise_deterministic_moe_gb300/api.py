@@ -82,6 +82,8 @@ def load() -> ctypes.CDLL:
         "moe_grouped_gemm_wgrad": ([P, P, P, I, I, I, I, P, I, LP, P, SZ, P], I),
         "dmoe_quantize_mxfp8": ([P, I, I, P, P, P], I),
         "dmoe_quantize_nvfp4": ([P, I, I, P, P, P, P, SZ, P], I),
+        "moe_grouped_gemm_dprob_mxfp8": ([P, P, P, P, P, I, I, I, I, P, P, P, I, I, P, P, LP, P, SZ, P], I),
+        "moe_grouped_gemm_dprob_nvfp4": ([P, P, P, P, P, P, P, I, I, I, I, P, P, P, I, I, P, P, LP, P, SZ, P], I),
         "moe_dprob_epilogue": ([P, P, P, P, I, I, I, I, I, P, P], I),
         "moe_dprob_combine": ([P, P, I, I, I, I, P, P], I),
         "dmoe_fingerprint_num_chunks": ([SZ, SZ], SZ),
@@ -386,6 +388,72 @@ def quantize_nvfp4(x: torch.Tensor, ws: torch.Tensor, packed=None, scales=None, 
                                     ws.numel(), _stream(stream))
     _check(st, "dmoe_quantize_nvfp4")
     return packed, scales, s_enc
+
+
+# ------------------------------------------------------------------ block-scaled grouped GEMM
+def _block_scaled(kind, Xq, Xs, Xg, Wq, Ws, Wg, expert_offsets, K, grad_out, row_src, topk, ws, out, slots, dprob,
+                  num_ctas, stream):
+    R = Xq.shape[0]
+    E = expert_offsets.numel() - 1
+    N = Wq.shape[1]
+    kb = K if kind == 0 else K // 2
+    sb = K // 32 if kind == 0 else K // 16
+    dev = Xq.device
+    _need(Xq, torch.uint8, "X codes", (R, kb))
+    _need(Xs, torch.uint8, "X scales", (R, sb))
+    _need(Wq, torch.uint8, "W codes", (E, N, kb))
+    _need(Ws, torch.uint8, "W scales", (E * N, sb))
+    _need(expert_offsets, torch.int32, "expert_offsets", (E + 1,))
+    if kind == 1:
+        _need(Xg, torch.float32, "X tensor scale", (1,))
+        _need(Wg, torch.float32, "W tensor scale", (1,))
+    if out is None:
+        out = torch.empty(R, N, dtype=torch.bfloat16, device=dev)
+    _need(out, torch.bfloat16, "expert_out", (R, N))
+    T = 0
+    if grad_out is not None:
+        T = R // topk
+        S = N // SLOT_COLS
+        if slots is None:
+            slots = torch.empty(S, R, dtype=torch.float32, device=dev)
+        if dprob is None:
+            dprob = torch.empty(T, topk, dtype=torch.float32, device=dev)
+        _need(grad_out, torch.bfloat16, "grad_out", (T, N))
+        _need(row_src, torch.int32, "row_src", (R,))
+        _need(slots, torch.float32, "slots", (S, R))
+        _need(dprob, torch.float32, "dprob", (T, topk))
+    lib = load()
+    if kind == 0:
+        st = lib.moe_grouped_gemm_dprob_mxfp8(_ptr(Xq), _ptr(Xs), _ptr(Wq), _ptr(Ws), _ptr(expert_offsets), R, E, K, N,
+                                              _ptr(out), _ptr(grad_out), _ptr(row_src), T, topk, _ptr(slots),
+                                              _ptr(dprob), _launch(num_ctas), _ptr(ws), ws.numel(), _stream(stream))
+        _check(st, "moe_grouped_gemm_dprob_mxfp8")
+    else:
+        st = lib.moe_grouped_gemm_dprob_nvfp4(_ptr(Xq), _ptr(Xs), _ptr(Xg), _ptr(Wq), _ptr(Ws), _ptr(Wg),
+                                              _ptr(expert_offsets), R, E, K, N, _ptr(out), _ptr(grad_out),
+                                              _ptr(row_src), T, topk, _ptr(slots), _ptr(dprob), _launch(num_ctas),
+                                              _ptr(ws), ws.numel(), _stream(stream))
+        _check(st, "moe_grouped_gemm_dprob_nvfp4")
+    return out, dprob, slots
+
+
+def grouped_gemm_dprob_mxfp8(X_q, X_scales, W_q, W_scales, expert_offsets, grad_out, row_src, topk: int, ws,
+                             out=None, slots=None, dprob=None, num_ctas: int = 0, stream=None):
+    """MXFP8 operands (E4M3 codes [R, K], [E, N, K]; E8M0 scales [R, K/32], [E*N, K/32]):
+    returns (expert_out bf16 [R, N], dprob, slots); grad_out None = forward only (dprob, slots None)."""
+    K = X_q.shape[1]
+    return _block_scaled(0, X_q, X_scales, None, W_q, W_scales, None, expert_offsets, K, grad_out, row_src, topk, ws,
+                         out, slots, dprob, num_ctas, stream)
+
+
+def grouped_gemm_dprob_nvfp4(X_packed, X_scales, X_s_enc, W_packed, W_scales, W_s_enc, expert_offsets, grad_out,
+                             row_src, topk: int, ws, out=None, slots=None, dprob=None, num_ctas: int = 0,
+                             stream=None):
+    """NVFP4 operands (packed E2M1 [R, K/2], [E, N, K/2]; E4M3 scales [R, K/16], [E*N, K/16]; fp32
+    tensor scales [1]): returns (expert_out bf16 [R, N], dprob, slots)."""
+    K = X_packed.shape[1] * 2
+    return _block_scaled(1, X_packed, X_scales, X_s_enc, W_packed, W_scales, W_s_enc, expert_offsets, K, grad_out,
+                         row_src, topk, ws, out, slots, dprob, num_ctas, stream)
 
 
 # ------------------------------------------------------------------ fingerprint

@@ -20,7 +20,8 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libdmoe.so")
 SOURCES = ["api.cu", "grouped_gemm.cu", "grouped_gemm_2sm.cu", "routing.cu", "dprob.cu", "fingerprint.cu",
-           "noalloc.cu", "dispatch.cu", "grouped_wgrad.cu", "quant.cu"]
+           "noalloc.cu", "dispatch.cu", "grouped_wgrad.cu", "quant.cu",
+           "grouped_gemm_bs.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

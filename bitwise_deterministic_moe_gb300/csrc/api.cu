@@ -379,6 +379,67 @@ dmoe_status dmoe_quantize_nvfp4(const void* x, int rows, int cols, uint8_t* pack
       launch_quantize_nvfp4(x, n, packed, scales, s_enc, scratch, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+// Block-scaled grouped GEMM (+ private-slot dprob when grad_out is given).
+static dmoe_status block_scaled_call(int kind, const uint8_t* Xq, const uint8_t* Xs, const float* Xg,
+                                     const uint8_t* Wq, const uint8_t* Ws, const float* Wg,
+                                     const int32_t* expert_offsets, int R, int E, int K, int N, void* expert_out,
+                                     const void* grad_out, const int32_t* row_src, int T, int topk, float* slots,
+                                     float* dprob, const dmoe_launch* launch, void* ws, size_t ws_bytes,
+                                     dmoe_stream_t stream) {
+  if (!Wq || !Ws || !expert_offsets) return DMOE_ERR_INVALID_ARG;
+  if (R < 0 || E < 1 || K < 1 || N < 1) return DMOE_ERR_INVALID_ARG;
+  if (R > 0 && (!Xq || !Xs || !expert_out)) return DMOE_ERR_INVALID_ARG;
+  if (kind == 1 && (!Xg || !Wg)) return DMOE_ERR_INVALID_ARG;
+  if (!aligned16(Xq) || !aligned16(Xs) || !aligned16(Wq) || !aligned16(Ws) || !aligned16(expert_out))
+    return DMOE_ERR_INVALID_ARG;
+  const int kmul = kind == 0 ? 512 : 256;   // whole 16-byte scale rows for the tensor maps
+  if (E > DMOE_MAX_EXPERTS || K % kmul != 0 || K > 65536 || N % DMOE_SLOT_COLS != 0 || N > 65536)
+    return DMOE_ERR_UNSUPPORTED;
+  if ((long long)E * N >= (1ll << 31)) return DMOE_ERR_UNSUPPORTED;
+  if (!ws || ws_bytes < DMOE_WS_STATUS_BYTES) return DMOE_ERR_WORKSPACE;
+  if (launch && launch->num_ctas < 0) return DMOE_ERR_INVALID_ARG;
+  if (grad_out) {
+    dmoe_status st = check_dprob_args(grad_out, row_src, R, T, topk);
+    if (st != DMOE_OK) return st;
+    if (!slots || !dprob) return DMOE_ERR_INVALID_ARG;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  BlockScaledArgs a{};
+  a.kind = kind;
+  a.Xq = Xq; a.Xs = Xs; a.Wq = Wq; a.Ws = Ws;
+  a.s_enc_x = Xg; a.s_enc_w = Wg;
+  a.offsets = expert_offsets;
+  a.R = R; a.E = E; a.K = K; a.N = N;
+  a.out = expert_out;
+  a.grad_out = grad_out; a.row_src = row_src; a.topk = topk;
+  a.slots = slots;
+  a.status = status_ptr(ws);
+  a.sched = sched_ptr(ws);
+  a.num_ctas = launch ? launch->num_ctas : 0;
+  if (launch_grouped_gemm_block_scaled(a, s) != cudaSuccess) return DMOE_ERR_CUDA;
+  if (!grad_out) return DMOE_OK;
+  return cuda_status(launch_dprob_combine(slots, row_src, R, N / DMOE_SLOT_COLS, dprob, s));
+}
+
+dmoe_status moe_grouped_gemm_dprob_mxfp8(const uint8_t* X_q, const uint8_t* X_scales, const uint8_t* W_q,
+                                         const uint8_t* W_scales, const int32_t* expert_offsets, int R, int E, int K,
+                                         int N, void* expert_out, const void* grad_out, const int32_t* row_src, int T,
+                                         int topk, float* slots, float* dprob, const dmoe_launch* launch, void* ws,
+                                         size_t ws_bytes, dmoe_stream_t stream) {
+  return block_scaled_call(0, X_q, X_scales, nullptr, W_q, W_scales, nullptr, expert_offsets, R, E, K, N, expert_out,
+                           grad_out, row_src, T, topk, slots, dprob, launch, ws, ws_bytes, stream);
+}
+
+dmoe_status moe_grouped_gemm_dprob_nvfp4(const uint8_t* X_packed, const uint8_t* X_scales, const float* X_s_enc,
+                                         const uint8_t* W_packed, const uint8_t* W_scales, const float* W_s_enc,
+                                         const int32_t* expert_offsets, int R, int E, int K, int N, void* expert_out,
+                                         const void* grad_out, const int32_t* row_src, int T, int topk, float* slots,
+                                         float* dprob, const dmoe_launch* launch, void* ws, size_t ws_bytes,
+                                         dmoe_stream_t stream) {
+  return block_scaled_call(1, X_packed, X_scales, X_s_enc, W_packed, W_scales, W_s_enc, expert_offsets, R, E, K, N,
+                           expert_out, grad_out, row_src, T, topk, slots, dprob, launch, ws, ws_bytes, stream);
+}
+
 size_t dmoe_fingerprint_num_chunks(size_t nbytes, size_t chunk_bytes) {
   if (chunk_bytes == 0) return 0;
   return (nbytes + chunk_bytes - 1) / chunk_bytes;

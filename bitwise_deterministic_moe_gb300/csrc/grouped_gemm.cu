@@ -577,6 +577,22 @@ bool make_tmap_bf16(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t col
   return r == CUDA_SUCCESS;
 }
 
+// 2-D tensor of `dtype` [rows, cols] with row pitch `row_bytes` (a multiple of
+// 16), box [box_rows, box_cols], with the given swizzle and L2 promotion.
+bool make_tmap_2d(CUtensorMap* m, const void* ptr, CUtensorMapDataType dtype, uint64_t rows, uint64_t cols,
+                  uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swizzle,
+                  CUtensorMapL2promotion promotion) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, dtype, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                  promotion, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // 2-D bf16 output [rows, cols] (cols contiguous, cols % 8 == 0) for TMA stores of
 // box [32, 32] (64-byte rows) from a 64-byte-swizzled staging buffer.
 bool make_tmap_bf16_store32(CUtensorMap* m, void* ptr, uint64_t rows, uint64_t cols) {

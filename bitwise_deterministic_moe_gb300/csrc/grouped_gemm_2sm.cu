@@ -34,6 +34,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tile_sched.cuh"
 
 namespace dmoe {
 
@@ -60,14 +61,6 @@ constexpr int NUM_THREADS = 32 * (SCHED_WARP + 1);
 constexpr int SLOT = DMOE_SLOT_COLS;
 constexpr int TQ = 4;
 constexpr int HEAVY_MT = 2;              // pair m-tiles (256 rows) per expert that make it compute-bound
-
-// A decoded tile as the scheduler queues it: cur = tile index (-1 = no more
-// tiles), e = expert, row0 = first row of the PAIR tile (the tile covers
-// row0 .. row0 + PM - 1), row_end = end of the expert's rows, columns
-// n0 .. n0 + BN - 1.
-struct alignas(16) QTile {
-  int cur, e, row0, row_end, n0, pad0, pad1, pad2;
-};
 
 struct alignas(16) Ctrl {
   uint64_t full[STAGES];                 // leader: both CTAs' halves of a stage landed
@@ -115,110 +108,6 @@ __device__ __forceinline__ uint64_t smem_desc_k128(uint32_t saddr) {
 // kind::f16: fp32 D, bf16 A and B, both K-major, M = 256 (the pair), N = 256.
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(BN >> 3) << 17) |
                             (uint32_t(PM >> 4) << 24);
-
-// The scheduler warp's expert tables, held in registers: lane l holds experts
-// e = 32 l + j (j = 0..31; E <= 1024), with off[e .. e + 32] (o), and the
-// exclusive prefixes of the pair m-tiles of heavy (hp) and light (cp)
-// experts before e.  All indices are compile-time after unrolling, so the
-// arrays stay in registers.
-struct ExpertTables {
-  int o[33];
-  int hp[32];
-  int cp[32];
-};
-
-// Loads the offsets, validates them (non-decreasing, off[0] = 0, off[E] = R)
-// and builds the prefixes; returns the units of each class through hu / lu
-// and whether the offsets are bad (warp-uniform).
-__device__ __forceinline__ bool build_tables(ExpertTables& t, const int32_t* offsets, int E, int R, int lane,
-                                             int& hu, int& lu) {
-  bool bad = false;
-#pragma unroll
-  for (int j = 0; j <= 32; ++j) {
-    const int e = 32 * lane + j;
-    t.o[j] = e <= E ? offsets[e] : 0;
-    if (e == E && t.o[j] != R) bad = true;
-  }
-  if (lane == 0 && t.o[0] != 0) bad = true;
-  int hsum = 0, csum = 0;
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const int e = 32 * lane + j;
-    int mt = 0;
-    if (e < E) {
-      if (t.o[j + 1] < t.o[j]) bad = true;
-      mt = t.o[j + 1] > t.o[j] ? (t.o[j + 1] - t.o[j] + PM - 1) / PM : 0;
-    }
-    t.hp[j] = hsum;
-    t.cp[j] = csum;
-    hsum += mt >= HEAVY_MT ? mt : 0;
-    csum += mt >= HEAVY_MT ? 0 : mt;
-  }
-  int hx = hsum, cx = csum;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const int hv = __shfl_up_sync(0xffffffffu, hx, d);
-    const int cv = __shfl_up_sync(0xffffffffu, cx, d);
-    if (lane >= d) {
-      hx += hv;
-      cx += cv;
-    }
-  }
-  hu = __shfl_sync(0xffffffffu, hx, 31);
-  lu = __shfl_sync(0xffffffffu, cx, 31);
-  hx -= hsum;
-  cx -= csum;
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    t.hp[j] += hx;
-    t.cp[j] += cx;
-  }
-  return __any_sync(0xffffffffu, bad);
-}
-
-// Same order as the single-CTA kernel, in units of one 256-row pair m-tile,
-// decoded by the whole scheduler warp from its register tables: the expert
-// is the largest e < E whose class prefix is <= u; the lanes whose first
-// expert qualifies form a prefix of the warp, the last of them holds e, and
-// within it the qualifying experts are a prefix of its 32.
-__device__ __forceinline__ QTile decode_tile_warp(int t, const ExpertTables& tb, int E, int NT, int H, int U,
-                                                  int lane) {
-  const int p = t / NT;
-  const int n_tile = t - p * NT;
-  const int i = int((long long)p * H / U);
-  const bool heavy = (long long)(p + 1) * H / U > i;
-  const int u = heavy ? i : p - i;
-  // the class's prefix selected with a mask, element by element, so that the
-  // tables are never addressed through a pointer (they must stay in registers)
-  const int hm = heavy ? -1 : 0;
-  int cnt = 0;
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const int pv = (tb.hp[j] & hm) | (tb.cp[j] & ~hm);
-    cnt += (32 * lane + j < E && pv <= u) ? 1 : 0;
-  }
-  const int seg = 31 - __clz(__ballot_sync(0xffffffffu, cnt > 0));   // lane 0 always (prefix 0 <= u)
-  int pe = 0, oe = 0, oe1 = 0;
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const int hj = j == cnt - 1 ? -1 : 0;
-    pe = (((tb.hp[j] & hm) | (tb.cp[j] & ~hm)) & hj) | (pe & ~hj);
-    oe = (tb.o[j] & hj) | (oe & ~hj);
-    oe1 = (tb.o[j + 1] & hj) | (oe1 & ~hj);
-  }
-  const int c = __shfl_sync(0xffffffffu, cnt, seg);
-  pe = __shfl_sync(0xffffffffu, pe, seg);
-  oe = __shfl_sync(0xffffffffu, oe, seg);
-  oe1 = __shfl_sync(0xffffffffu, oe1, seg);
-  QTile q;
-  q.cur = t;
-  q.e = 32 * seg + c - 1;
-  q.row0 = oe + (u - pe) * PM;
-  q.row_end = oe1;
-  q.n0 = n_tile * BN;
-  q.pad0 = q.pad1 = q.pad2 = 0;
-  return q;
-}
 
 __device__ __forceinline__ uint4 shfl_xor_u4(const uint4& v, int m) {
   uint4 r;
@@ -455,7 +344,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
       // slot; the next claim is in flight meanwhile.
       ExpertTables tb;
       int units_heavy = 0, units_light = 0;
-      const bool bad = build_tables(tb, p.offsets, E, p.R, lane, units_heavy, units_light);
+      const bool bad = build_tables<PM, HEAVY_MT>(tb, p.offsets, E, p.R, lane, units_heavy, units_light);
       if (bad && lane == 0) record_error(p.status, DMOE_ERR_ROUTING);
       const int units = units_heavy + units_light;
       const int total_tiles = bad ? 0 : units * p.NT;
@@ -469,7 +358,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
         if (cur >= 0 && lane == 0) nxt = n_pairs + atomicAdd(p.sched, 1);
         QTile q{};
         q.cur = -1;
-        if (cur >= 0) q = decode_tile_warp(cur, tb, E, p.NT, units_heavy, units, lane);
+        if (cur >= 0) q = decode_tile_warp<PM, BN>(cur, tb, E, p.NT, units_heavy, units, lane);
         if (!pwarp_wait<true>(smem_u32(&c.tq_empty[qs]), uint32_t((qi / TQ) & 1) ^ 1u, c, p, peer_abort, lane))
           break;
         if (lane == 0) {

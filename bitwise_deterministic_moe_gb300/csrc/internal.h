@@ -33,6 +33,28 @@ struct GemmArgs {
 cudaError_t launch_grouped_gemm(GemmMode mode, const GemmArgs& a, cudaStream_t stream);       // CTA pairs
 cudaError_t launch_grouped_gemm_1sm(GemmMode mode, const GemmArgs& a, cudaStream_t stream);   // single CTAs
 
+// block-scaled grouped GEMM (MXFP8 / NVFP4 operands) with the slot epilogue
+struct BlockScaledArgs {
+  int kind;                   // 0 = MXFP8 (E4M3 + E8M0 per 32), 1 = NVFP4 (packed E2M1 + E4M3 per 16 + tensor scale)
+  const void* Xq;             // [R, K] codes (MXFP8) or [R, K/2] packed (NVFP4)
+  const void* Xs;             // [R, K/32] or [R, K/16] scale bytes
+  const void* Wq;             // [E*N, K] or [E*N, K/2]
+  const void* Ws;             // [E*N, K/32] or [E*N, K/16]
+  const float* s_enc_x;       // NVFP4 tensor scales (device fp32), else null
+  const float* s_enc_w;
+  const int32_t* offsets;     // [E+1]
+  int R, E, K, N;
+  void* out;                  // bf16 [R, N]
+  const void* grad_out;       // bf16 [T, N]; null = forward only
+  const int32_t* row_src;     // [R]
+  int topk;
+  float* slots;               // [N/128, R]
+  int* status;
+  int* sched;
+  int num_ctas;
+};
+cudaError_t launch_grouped_gemm_block_scaled(const BlockScaledArgs& a, cudaStream_t stream);
+
 // grouped-GEMM weight gradient: dW[e] (+)= dY_e^T X_e
 struct WgradArgs {
   const void* X;              // bf16 [R, K]

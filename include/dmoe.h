@@ -377,6 +377,53 @@ dmoe_status dmoe_quantize_nvfp4(const void* x, int rows, int cols, uint8_t* pack
                                 void* ws, size_t ws_bytes, dmoe_stream_t stream);
 
 /*
+ * Block-scaled grouped GEMM with the private-slot dprob epilogue: the expert
+ * GEMM of moe_grouped_gemm_dprob with MXFP8 or NVFP4 operands, in the
+ * encodings dmoe_quantize_mxfp8 / dmoe_quantize_nvfp4 produce ("NVIDIA fait
+ * passer le déterminisme bit à bit de Megatron Core à 2432 GPU ...", section
+ * "Méthodologie de débogage du non-déterminisme": MXFP8 and NVFP4 values and
+ * scale buffers are part of the fingerprinted path; "Nemotron 3 Ultra 的 tech
+ * report ...", NVFP4 pretraining section).
+ *   expert_out[r, n] = bf16_rne( sum_c dec(X)[r, c] * dec(W[e])[n, c] )
+ * for rows r of expert e, with dec the block-scaled decoding:
+ *   MXFP8: dec = E4M3(code) * 2^(scale - 127), one E8M0 scale per 32 values
+ *          of a row (scale 0xFF decodes to NaN);
+ *   NVFP4: dec = E2M1(code) * E4M3(scale) / S_enc, one E4M3 scale per 16
+ *          values, S_enc the operand's fp32 tensor scale.
+ * When grad_out is given, the slots and dprob follow exactly as in
+ * moe_grouped_gemm_dprob (128-column private slots from the stored bf16
+ * output, fixed in-slot tree, fixed-order combine); grad_out == NULL computes
+ * expert_out only (row_src, T, topk, slots and dprob are then ignored).
+ *   MXFP8: X_q uint8 [R, K], X_scales uint8 [R, K/32], W_q uint8 [E, N, K],
+ *          W_scales uint8 [E*N, K/32]; K % 512 == 0.
+ *   NVFP4: X_packed uint8 [R, K/2] (element 2i in the low nibble), X_scales
+ *          uint8 [R, K/16], X_s_enc fp32 [1] (device); W_packed uint8
+ *          [E, N, K/2], W_scales uint8 [E*N, K/16], W_s_enc fp32 [1];
+ *          K % 256 == 0.
+ *   expert_offsets int32 [E+1], expert_out bf16 [R, N], grad_out bf16 [T, N],
+ *   row_src int32 [R], slots fp32 [N/128, R], dprob fp32 [T, topk].
+ * All pointers are device memory owned by the caller, operand and scale
+ * arrays 16-byte aligned.  1 <= E <= DMOE_MAX_EXPERTS, N % 128 == 0,
+ * K, N <= 65536, E * N < 2^31; other shapes return DMOE_ERR_UNSUPPORTED.
+ * Accumulation is fp32 on the tensor cores in a fixed k order, so results
+ * are bitwise identical for any num_ctas and any stream; device-side errors
+ * (offsets, row_src) go to the workspace status word as in
+ * moe_grouped_gemm_dprob.  launch->flags is ignored (one kernel: 128 x 128
+ * tiles on single CTAs).
+ */
+dmoe_status moe_grouped_gemm_dprob_mxfp8(const uint8_t* X_q, const uint8_t* X_scales, const uint8_t* W_q,
+                                         const uint8_t* W_scales, const int32_t* expert_offsets, int R, int E, int K,
+                                         int N, void* expert_out, const void* grad_out, const int32_t* row_src, int T,
+                                         int topk, float* slots, float* dprob, const dmoe_launch* launch, void* ws,
+                                         size_t ws_bytes, dmoe_stream_t stream);
+dmoe_status moe_grouped_gemm_dprob_nvfp4(const uint8_t* X_packed, const uint8_t* X_scales, const float* X_s_enc,
+                                         const uint8_t* W_packed, const uint8_t* W_scales, const float* W_s_enc,
+                                         const int32_t* expert_offsets, int R, int E, int K, int N, void* expert_out,
+                                         const void* grad_out, const int32_t* row_src, int T, int topk, float* slots,
+                                         float* dprob, const dmoe_launch* launch, void* ws, size_t ws_bytes,
+                                         dmoe_stream_t stream);
+
+/*
  * Chunk-wise tensor fingerprint ("NVIDIA fait passer ...", section "Méthodologie
  * de débogage du non-déterminisme": fingerprints computed on the GPU, with
  * shape, dtype and element count recorded, chunk-wise for order-sensitive

@@ -39,6 +39,16 @@ Contents and the passage each part follows:
   encoded values and scale buffers the pages fingerprint ("NVIDIA fait passer
   ...", section "Méthodologie de débogage du non-déterminisme"); E4M3, E2M1
   and E8M0 decoded and encoded from their format definitions.
+* ``mxfp8_decode`` / ``nvfp4_decode`` / ``block_scaled_rows`` -- the expert
+  GEMM on block-scaled operands: each operand decoded to binary64 from its
+  codes and scales by the format definitions, then the same grouped GEMM,
+  bf16 rounding, private-slot partials and dprob as ``expert_rows``
+  ("NVIDIA fait passer ...", section "Méthodologie de débogage du
+  non-déterminisme", for MXFP8 / NVFP4 operands in the fingerprinted path;
+  "Nemotron 3 Ultra 的 tech report ...", NVFP4 pretraining section, for NVFP4
+  GEMMs; "Trillion-Parameter Pretraining ...", section "Interpretation", for
+  the slots).  The GEMM step is a binary64 matrix product (a library
+  primitive).
 * ``fingerprint`` -- chunk-wise tensor fingerprint with a header over dtype,
   shape and numel (same French page, section "Méthodologie de débogage du
   non-déterminisme": fingerprints computed on the GPU with shape, dtype and
@@ -429,6 +439,67 @@ def nvfp4_quantize(x_bits, amax=None):
     q = e2m1_encode(r.astype(np.float64)).reshape(rows, cols)
     packed = (q[:, 0::2] & 0xF) | ((q[:, 1::2] & 0xF) << 4)
     return packed.astype(np.uint8), scales, s_enc
+
+
+def mxfp8_decode(codes, scales) -> np.ndarray:
+    """binary64 values of an MXFP8 tensor: E4M3(code) * 2^(scale - 127) for each
+    run of 32 consecutive values of a row sharing one E8M0 scale byte (OCP
+    Microscaling Formats v1.0; scale 0xFF encodes NaN).
+    codes uint8 [rows, cols], scales uint8 [rows, cols/32]."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    scales = np.asarray(scales, dtype=np.uint8)
+    rows, cols = codes.shape
+    assert scales.shape == (rows, cols // MX_BLOCK)
+    sc = np.where(scales == 0xFF, np.nan, np.exp2(scales.astype(np.float64) - 127.0))
+    v = e4m3_value(codes).reshape(rows, cols // MX_BLOCK, MX_BLOCK) * sc[..., None]
+    return v.reshape(rows, cols)
+
+
+def nvfp4_decode(packed, scales, s_enc) -> np.ndarray:
+    """binary64 values of an NVFP4 tensor: E2M1(code) * E4M3(scale) / S_enc,
+    one E4M3 scale per run of 16 consecutive values of a row, S_enc the
+    tensor's fp32 encode scale; two codes per byte, element 2i in the low nibble.
+    packed uint8 [rows, cols/2], scales uint8 [rows, cols/16]."""
+    packed = np.asarray(packed, dtype=np.uint8)
+    scales = np.asarray(scales, dtype=np.uint8)
+    rows, half = packed.shape
+    cols = 2 * half
+    assert scales.shape == (rows, cols // NV_BLOCK)
+    codes = np.empty((rows, cols), dtype=np.uint8)
+    codes[:, 0::2] = packed & 0xF
+    codes[:, 1::2] = packed >> 4
+    v = e2m1_value(codes).reshape(rows, cols // NV_BLOCK, NV_BLOCK) * e4m3_value(scales)[..., None]
+    return v.reshape(rows, cols) / float(np.float32(s_enc))
+
+
+def block_scaled_rows(Xd, W_decoded, off, rows, G=None, row_src=None, topk=1, slot_width=SLOT_WIDTH):
+    """The grouped GEMM on decoded operands for the requested permuted rows:
+    Y[i, n] = sum_c Xd[rows[i], c] * Wd[e][n, c] in binary64 (e = the expert whose
+    range holds rows[i]; Wd[e] = W_decoded(e), [N, K] binary64), Yb = bf16_rne(Y),
+    and, when G is given, the slot partials P [nrows, S] and dots D [nrows] of the
+    stored Yb exactly as for bf16 operands.  Returns (Y, Yb, P, D)."""
+    Xd = np.asarray(Xd, dtype=np.float64)
+    off = np.asarray(off, dtype=np.int64)
+    rows = np.asarray(rows, dtype=np.int64)
+    if rows.size and (rows.min() < 0 or rows.max() >= off[-1]):
+        raise ValueError("a requested row is not covered by any expert")
+    experts = np.searchsorted(off, rows, side="right") - 1
+    Y = None
+    for e in np.unique(experts):
+        sel = np.where(experts == e)[0]
+        We = np.asarray(W_decoded(int(e)), dtype=np.float64)
+        Ye = Xd[rows[sel]] @ We.T
+        if Y is None:
+            Y = np.empty((rows.size, We.shape[0]), dtype=np.float64)
+        Y[sel] = Ye
+    if Y is None:
+        return np.zeros((0, 0)), np.zeros((0, 0), np.uint16), None, None
+    Yb = bf16_rne(Y)
+    P = D = None
+    if G is not None:
+        src = np.asarray(row_src, dtype=np.int32)[rows]
+        P, D = dprob_from_output(G, Yb, src, topk, rows=np.arange(rows.size), slot_width=slot_width)
+    return Y, Yb, P, D
 
 
 # --------------------------------------------------------------------------

@@ -59,6 +59,13 @@ def check_rows_against_oracle(prob, out, slots, dprob, rows):
     rows = np.asarray(rows, dtype=np.int64)
     Y, Yb, P, D = oracle.expert_rows(inp.X, inp.W, off_ref, rows, G=inp.G, row_src=src_ref, topk=cfg.topk,
                                      want_Y=True, want_Yb=True, want_P=True, want_D=True)
+    return compare_rows(out, slots, dprob, rows, Y, Yb, P, D, src_ref, inp.G, cfg.topk)
+
+
+def compare_rows(out, slots, dprob, rows, Y, Yb, P, D, src_ref, G_bits, topk):
+    """The tolerance checks of check_rows_against_oracle for reference values
+    (Y binary64, Yb bf16 bits, P, D binary64) computed by the oracle for `rows`."""
+    rows = np.asarray(rows, dtype=np.int64)
     idx = torch.from_numpy(rows).to(out.device)
     got_y = oracle.bf16_to_f64(bf16_host_bits(out.index_select(0, idx)))
     rowmax = np.maximum(np.abs(Y).max(axis=1, keepdims=True), 1e-30)
@@ -67,8 +74,8 @@ def check_rows_against_oracle(prob, out, slots, dprob, rows):
     if slots is None and dprob is None:
         return err_y.max()
     # per-element magnitude scales: |G[t(r), n]| * |Yb[r, n]| summed per slot and per row
-    tok = src_ref[rows].astype(np.int64) // cfg.topk
-    mag = np.abs(oracle.bf16_to_f64(np.asarray(inp.G)[tok])) * np.abs(oracle.bf16_to_f64(Yb))
+    tok = src_ref[rows].astype(np.int64) // topk
+    mag = np.abs(oracle.bf16_to_f64(np.asarray(G_bits)[tok])) * np.abs(oracle.bf16_to_f64(Yb))
     slot_mag = mag.reshape(rows.size, -1, 128).sum(axis=2)
     row_mag = mag.sum(axis=1)
     if slots is not None:
