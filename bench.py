@@ -317,6 +317,55 @@ def wgrad_measure(api, cfg, X, dY, off, ws, timed, dev, iters):
             "tensor_frac": flops / (ms * 1e-3) / 1e12 / pk["bf16_tflops"]}
 
 
+def block_scaled_measure(api, cfg, X, W, G, off, src, ws, timed, iters):
+    """The block-scaled grouped GEMM + slot dprob on the workload's operands
+    encoded as MXFP8 and as NVFP4 (encoding outside the timed launches).
+    Peaks: the measured bf16 burst figure times the nominal dense ratio of the
+    format (fp8 4.5 / bf16 2.25 = 2; fp4 13.5 / 2.25 = 6 PFLOP/s on GB300).
+    Algorithmic bytes: codes and scales of X and of the used experts' W read
+    once, expert_out written, grad_out read once, slots written and read,
+    row_src and dprob."""
+    import torch
+    pk, _ = peaks()
+    counts = np.diff(off.cpu().numpy())
+    used = int((counts > 0).sum())
+    R, K, N, E, T, S = cfg.R, cfg.K, cfg.N, cfg.E, cfg.T, cfg.S
+    flops = 2.0 * R * K * N
+    W2 = W.view(E * N, K)
+    res = {}
+    out = torch.empty(R, N, dtype=torch.bfloat16, device=X.device)
+    sl = torch.empty(S, R, dtype=torch.float32, device=X.device)
+    dp = torch.empty(T, cfg.topk, dtype=torch.float32, device=X.device)
+    for kind, ratio in (("mxfp8", 2.0), ("nvfp4", 6.0)):
+        if kind == "mxfp8":
+            xq, xs = api.quantize_mxfp8(X)
+            wq, wsc = api.quantize_mxfp8(W2)
+            fn = lambda: api.grouped_gemm_dprob_mxfp8(xq, xs, wq.view(E, N, K), wsc, off, G, src, cfg.topk, ws,
+                                                      out=out, slots=sl, dprob=dp)
+            opb = R * K + R * K // 32 + used * N * (K + K // 32)
+        else:
+            xq, xs, xg = api.quantize_nvfp4(X, ws)
+            wq, wsc, wg = api.quantize_nvfp4(W2, ws)
+            fn = lambda: api.grouped_gemm_dprob_nvfp4(xq, xs, xg, wq.view(E, N, K // 2), wsc, wg, off, G, src,
+                                                      cfg.topk, ws, out=out, slots=sl, dprob=dp)
+            opb = R * K // 2 + R * K // 16 + used * N * (K // 2 + K // 16)
+        ms = timed(fn, iters)
+        if api.read_status(ws) != 0:
+            raise RuntimeError(f"device status set while timing the {kind} GEMM")
+        b = opb + R * N * 2 + T * N * 2 + 2 * S * R * 4 + 2 * R * 4
+        tf = flops / (ms * 1e-3) / 1e12
+        peak = pk["bf16_tflops"] * ratio
+        res[kind] = {"ms": ms, "tflops": tf, "peak_tflops": peak,
+                     "peak_source": f"measured bf16 burst x {ratio:g} (nominal dense ratio)",
+                     "tensor_frac": tf / peak, "algorithmic_bytes": b, "achieved_gbs": b / (ms * 1e-3) / 1e9,
+                     "hbm_frac": b / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+                     "kernel": "grouped_gemm_bs_kernel (128x128 tiles, single CTA)"}
+        del xq, xs, wq, wsc
+    del out, sl, dp
+    torch.cuda.empty_cache()
+    return res
+
+
 def passes_measure(api, cfg, out, slots, src, off, G, timed, iters):
     """The HBM passes of the path on buffers of the workload: the chunk
     fingerprint of expert_out (R*N*2 bytes, larger than L2), the fixed-order
@@ -588,6 +637,8 @@ def run_ours(args):
                                                               args.tax_iters)
     wg = None if args.skip_wgrad else wgrad_measure(api, cfg, X, out, off, ws, timed, dev, args.tax_iters)
     qz = None if args.skip_quant else quant_measure(api, X, ws, timed, args.tax_iters)
+    bsg = None if args.skip_block_scaled else block_scaled_measure(api, cfg, X, W, G, off, src, ws, timed,
+                                                                    args.tax_iters)
     hp = passes_measure(api, cfg, out, slots, src, off, G, timed, max(args.tax_iters, 20))
     hp["slot_combine"].update({"l2": "back to back, buffer smaller than L2"})
     hp["slot_combine_latent_cold"] = combine_pass(slots, src, cfg)
@@ -736,6 +787,7 @@ def run_ours(args):
         "dispatch_combine": around,
         "wgrad": wg,
         "quantize": qz,
+        "block_scaled_gemm": bsg,
         "hbm_passes": hp,
         "e2e": e2e,
         "clocks": clocks,
@@ -820,6 +872,7 @@ def main():
     ap.add_argument("--skip-dispatch", action="store_true")
     ap.add_argument("--skip-wgrad", action="store_true")
     ap.add_argument("--skip-quant", action="store_true")
+    ap.add_argument("--skip-block-scaled", action="store_true")
     ap.add_argument("--num-ctas", type=int, default=0, help="persistent CTAs of the GEMM (0 = all resident)")
     ap.add_argument("--kernel", default="auto", choices=sorted(KERNEL_FLAGS),
                     help="GEMM kernel: the call's own choice, or force one (same bits)")

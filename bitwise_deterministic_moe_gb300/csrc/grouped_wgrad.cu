@@ -20,7 +20,7 @@
 // boxes LBO = 8 KB apart along M/N, 8-row groups SBO = 1 KB apart along the
 // reduction, 2 KB per 16-row MMA step.
 //
-// Design (one CTA per SM, persistent, warp-specialised, 320 threads):
+// Design (one CTA per SM, persistent, warp-specialised, 352 threads):
 //   warp 0     TMA producer: per stage dY [64 r x 128 n] and X [64 r x 256 c].
 //   warp 1     tcgen05.mma issuer (lane 0): 128x256x16 MMAs, fp32 in tensor
 //              memory (2 x 256 columns).  In a tile's last stage only the
@@ -29,6 +29,11 @@
 //              next expert, so no row is ever counted twice.
 //   warps 2-9  epilogue: tensor memory -> registers -> swizzled shared memory ->
 //              TMA tensor stores of dW (add-reduce stores in accumulate mode).
+//   warp 10    tile scheduler: claims tiles and decodes each into (expert,
+//              rows, n and c offsets) a few tiles ahead of use, so the
+//              producer goes from one tile's last row block to the next
+//              tile's first without a pause (light experts' tiles are only one
+//              or two row blocks long).
 // Tiles (one 128 x 256 block of one expert's dW) of experts with many rows come
 // first, then the rest, each class in expert order, handed out dynamically.
 #include <cuda.h>
@@ -57,12 +62,18 @@ constexpr int ACC_BUFS = 2;
 constexpr int TMEM_COLS = ACC_BUFS * BN;
 constexpr int EPI_WARP0 = 2;
 constexpr int EPI_WARPS = 8;
-constexpr int NUM_THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
+constexpr int SCHED_WARP = EPI_WARP0 + EPI_WARPS;
+constexpr int NUM_THREADS = 32 * (SCHED_WARP + 1);
 constexpr int TQ = 4;
 constexpr int HEAVY_KB = 16;             // experts with >= 16 row blocks (1024 rows) go first
 constexpr int STG_BYTES = 32 * 64;       // per epilogue warp: 32 rows x 16 fp32
 
-struct alignas(8) Ctrl {
+// A decoded tile as the scheduler queues it (cur = -1: no more tiles).
+struct alignas(16) WTile {
+  int cur, e, row0, rows, n0, c0, pad0, pad1;
+};
+
+struct alignas(16) Ctrl {
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
   uint64_t acc_full[ACC_BUFS];
@@ -70,7 +81,7 @@ struct alignas(8) Ctrl {
   uint64_t mma_done;
   uint64_t tq_full[TQ];
   uint64_t tq_empty[TQ];
-  int tq_tile[TQ];
+  WTile tq[TQ];
   uint32_t tmem_base;
   int abort;
   int off[DMOE_MAX_EXPERTS + 1];
@@ -108,29 +119,31 @@ __device__ __forceinline__ uint64_t smem_desc_mn128(uint32_t saddr) {
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | (1u << 16) |
                             (uint32_t(BN >> 3) << 17) | (uint32_t(BM >> 4) << 24);
 
-struct Tile {
-  int e, row0, rows, n0, c0;
-};
-
 // Tile t: heavy experts' tiles first (expert order), then the others; inside
 // an expert, the n-tile varies fastest.  Only the timing depends on it.
-__device__ __forceinline__ Tile decode_tile(int t, const Ctrl& c, int E, int NTn, int NTc, int heavy_tiles) {
+// Decoded by the whole scheduler warp: the expert is the largest e < E whose
+// class prefix count is <= u (two ballots over the shared tables, E <= 1024).
+__device__ __forceinline__ WTile decode_tile_warp(int t, const Ctrl& c, int E, int NTn, int NTc, int heavy_tiles,
+                                                  int lane) {
   const int per = NTn * NTc;
   const bool heavy = t < heavy_tiles;
   const int u = heavy ? t / per : (t - heavy_tiles) / per;
   const int j = heavy ? t % per : (t - heavy_tiles) % per;
   const int* pre = heavy ? c.hp : c.lp;
-  int lo = 0, hi = E;
-  while (hi - lo > 1) {
-    int mid = (lo + hi) >> 1;
-    if (pre[mid] <= u) lo = mid; else hi = mid;
-  }
-  Tile tl;
-  tl.e = lo;
-  tl.row0 = c.off[lo];
-  tl.rows = c.off[lo + 1] - c.off[lo];
+  const int e1 = lane * 32;
+  const unsigned m1 = __ballot_sync(0xffffffffu, e1 < E && pre[e1] <= u);   // lane 0 always (pre[0] = 0)
+  const int seg = 31 - __clz(m1);
+  const int e2 = seg * 32 + lane;
+  const unsigned m2 = __ballot_sync(0xffffffffu, e2 < E && pre[e2] <= u);
+  const int e = seg * 32 + (31 - __clz(m2));
+  WTile tl;
+  tl.cur = t;
+  tl.e = e;
+  tl.row0 = c.off[e];
+  tl.rows = c.off[e + 1] - c.off[e];
   tl.n0 = (j % NTn) * BM;
   tl.c0 = (j / NTn) * BN;
+  tl.pad0 = tl.pad1 = 0;
   return tl;
 }
 
@@ -158,7 +171,7 @@ grouped_wgrad_kernel(const __grid_constant__ CUtensorMap tmap_dy, const __grid_c
     mbar_init(smem_u32(&c.mma_done), 1);
     for (int i = 0; i < TQ; ++i) {
       mbar_init(smem_u32(&c.tq_full[i]), 1);
-      mbar_init(smem_u32(&c.tq_empty[i]), 1 + EPI_WARPS);
+      mbar_init(smem_u32(&c.tq_empty[i]), 2 + EPI_WARPS);   // producer, MMA warp, epilogue warps
     }
     c.abort = 0;
     fence_barrier_init();
@@ -220,16 +233,12 @@ grouped_wgrad_kernel(const __grid_constant__ CUtensorMap tmap_dy, const __grid_c
       int issued_total = 0;
       int stage = 0;
       uint32_t ph = 0;
-      int tile = blockIdx.x;
       for (int qi = 0;; ++qi) {
         const int qs = qi % TQ;
-        if (!mbar_wait(smem_u32(&c.tq_empty[qs]), uint32_t((qi / TQ) & 1) ^ 1u, &c.abort, p.status, p.wait_ns)) break;
-        const int cur = tile < total_tiles ? tile : -1;
-        c.tq_tile[qs] = cur;
-        mbar_arrive(smem_u32(&c.tq_full[qs]));
-        if (cur < 0) break;
-        tile = int(gridDim.x) + atomicAdd(p.sched, 1);
-        const Tile tl = decode_tile(cur, c, E, p.NTn, p.NTc, heavy_tiles);
+        if (!mbar_wait(smem_u32(&c.tq_full[qs]), uint32_t((qi / TQ) & 1), &c.abort, p.status, p.wait_ns)) break;
+        const WTile tl = c.tq[qs];
+        mbar_arrive(smem_u32(&c.tq_empty[qs]));
+        if (tl.cur < 0) break;
         const int KB = (tl.rows + BK - 1) / BK;
         bool ok = true;
         for (int kb = 0; kb < KB; ++kb) {
@@ -264,11 +273,10 @@ grouped_wgrad_kernel(const __grid_constant__ CUtensorMap tmap_dy, const __grid_c
     for (int qi = 0;; ++qi) {
       const int qs = qi % TQ;
       if (!warp_wait(smem_u32(&c.tq_full[qs]), uint32_t((qi / TQ) & 1), &c.abort, p.status, lane, p.wait_ns)) break;
-      const int cur = c.tq_tile[qs];
+      const WTile tl = c.tq[qs];
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&c.tq_empty[qs]));
-      if (cur < 0) break;
-      const Tile tl = decode_tile(cur, c, E, p.NTn, p.NTc, heavy_tiles);
+      if (tl.cur < 0) break;
       const int KB = (tl.rows + BK - 1) / BK;
       if (KB == 0) continue;   // an expert without rows: the epilogue writes zeros
       if (!warp_wait(smem_u32(&c.acc_empty[acc]), aph ^ 1u, &c.abort, p.status, lane, p.wait_ns)) break;
@@ -320,6 +328,29 @@ grouped_wgrad_kernel(const __grid_constant__ CUtensorMap tmap_dy, const __grid_c
       mbar_wait_drain(smem_u32(&c.mma_done), 0, p.wait_ns / 4);
     }
     __syncwarp();
+  } else if (warp == SCHED_WARP) {
+    // -------------------------------------------------- tile scheduler (one warp)
+    // first tile = blockIdx.x, then the global counter; each claimed tile is
+    // decoded while its queue slot is still in use and queued as soon as it
+    // frees, with the next claim in flight meanwhile
+    int tile = int(blockIdx.x);
+    for (int qi = 0;; ++qi) {
+      const int qs = qi % TQ;
+      const int cur = tile < total_tiles ? tile : -1;
+      int nxt = 0;
+      if (cur >= 0 && lane == 0) nxt = int(gridDim.x) + atomicAdd(p.sched, 1);
+      WTile q{};
+      q.cur = -1;
+      if (cur >= 0) q = decode_tile_warp(cur, c, E, p.NTn, p.NTc, heavy_tiles, lane);
+      if (!warp_wait(smem_u32(&c.tq_empty[qs]), uint32_t((qi / TQ) & 1) ^ 1u, &c.abort, p.status, lane, p.wait_ns))
+        break;
+      if (lane == 0) {
+        c.tq[qs] = q;
+        mbar_arrive(smem_u32(&c.tq_full[qs]));
+      }
+      if (cur < 0) break;
+      tile = __shfl_sync(0xffffffffu, nxt, 0);
+    }
   } else {
     // -------------------------------------------------- epilogue (8 warps)
     // Warp w reads TMEM lanes 32*(w%4)..+31 (dW rows n0 + 32q ..); warps 2-5
@@ -338,11 +369,10 @@ grouped_wgrad_kernel(const __grid_constant__ CUtensorMap tmap_dy, const __grid_c
     for (int qi = 0;; ++qi) {
       const int qs = qi % TQ;
       if (!warp_wait(smem_u32(&c.tq_full[qs]), uint32_t((qi / TQ) & 1), &c.abort, p.status, lane, p.wait_ns)) break;
-      const int cur = c.tq_tile[qs];
+      const WTile tl = c.tq[qs];
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&c.tq_empty[qs]));
-      if (cur < 0) break;
-      const Tile tl = decode_tile(cur, c, E, p.NTn, p.NTc, heavy_tiles);
+      if (tl.cur < 0) break;
       const int col0 = tl.c0 + h * 128;
       float* dw_rows = p.dW + (size_t(tl.e) * p.N + tl.n0 + q * 32) * size_t(p.K);
       if (tl.rows == 0) {
@@ -402,7 +432,9 @@ grouped_wgrad_kernel(const __grid_constant__ CUtensorMap tmap_dy, const __grid_c
     tmem_dealloc(tmem_base, TMEM_COLS);
   }
   if (tid == 0) {
-    // the last CTA to finish zeroes the tile counters for the next launch
+    // every counter fetch of this CTA (made by its scheduler warp) has
+    // returned before the barrier above; the last CTA to finish zeroes the
+    // tile counters for the next launch
     __threadfence();
     if (atomicAdd(p.sched + 1, 1) == int(gridDim.x) - 1) {
       atomicExch(p.sched, 0);
