@@ -21,22 +21,25 @@
 //          tcgen05.mma .kind::mxf4nvf4.block_scale.scale_vec::4X, K = 64 per
 //          MMA, and the epilogue multiplies by 1 / (S_enc(X) * S_enc(W))
 //
-// Design (one CTA per SM, persistent, 256 threads), in the shape of the bf16
+// Design (one CTA per SM, persistent, 384 threads), in the shape of the bf16
 // single-CTA kernel with 128 x 128 tiles (one tile = one slot):
 //   warp 0  TMA producer: per stage the A and B operand boxes (128 rows x 128
 //           bytes, 128-byte swizzle) and two 128-row x 16-byte boxes of their
 //           scale bytes.
 //   warp 1  MMA issuer (one thread): copies the stage's scale blocks into
 //           tensor memory (tcgen05.cp .32x128b.warpx4), then four block-scaled
-//           MMAs; fp32 accumulators double-buffered in tensor memory.
-//   warps 2-5  epilogue (one per TMEM lane quarter, 32 rows x 128 columns):
-//           bf16 rounding, expert_out stores and the slot's dot products.
-//   warp 6  scale transposer: rearranges each stage's scale box into the
+//           MMAs; three fp32 accumulators in tensor memory.
+//   warps 2-9  epilogue, two groups of four (one warp per TMEM lane quarter,
+//           32 rows x 128 columns): the groups take alternate tiles, so two
+//           tiles' epilogues (bf16 rounding, expert_out stores, the slot's dot
+//           products) run while the next tile accumulates -- a tile is only
+//           4 (NVFP4) or 8 (MXFP8) short stages at K = 1024.
+//   warp 10 scale transposer: rearranges each stage's scale box into the
 //           layout the tensor core reads -- the scale of operand row r sits
 //           in tensor-memory lane r (A) or r mod 32 (B), column r / 32 -- as
 //           32-row x 16-byte blocks whose word (j, c) is the scale of tile
 //           row 32c + j.
-//   warp 7  tile scheduler (expert tables in registers, decoded tiles queued
+//   warp 11 tile scheduler (expert tables in registers, decoded tiles queued
 //           ahead of use).
 // Each output element is produced by one tile with a fixed k order and a
 // fixed epilogue tree, so results do not depend on the grid, the stream or
@@ -59,42 +62,52 @@ namespace {
 constexpr int BM = 128;                       // rows per tile (UMMA M)
 constexpr int BN = 128;                       // columns per tile (UMMA N) = one slot
 constexpr int ROWB = 128;                     // operand bytes per row per stage (one swizzle row)
-constexpr int STAGES = 5;
 constexpr int A_BYTES = BM * ROWB;            // 16 KB
 constexpr int B_BYTES = BN * ROWB;            // 16 KB
 constexpr int SFBOX_BYTES = 128 * 16;         // TMA box of scale bytes: 128 rows x 16 bytes
 constexpr int SFBLK_BYTES = 32 * 16;          // one tcgen05.cp block: 32 rows x 16 bytes
-constexpr int MAX_BLK = 4;                    // scale blocks per operand and stage (NVFP4: one per MMA)
-constexpr int OFF_B = A_BYTES;
-constexpr int OFF_SFA_BOX = A_BYTES + B_BYTES;
-constexpr int OFF_SFB_BOX = OFF_SFA_BOX + SFBOX_BYTES;
-constexpr int OFF_SFA_BLK = OFF_SFB_BOX + SFBOX_BYTES;
-constexpr int OFF_SFB_BLK = OFF_SFA_BLK + MAX_BLK * SFBLK_BYTES;
-constexpr int STAGE_BYTES = OFF_SFB_BLK + MAX_BLK * SFBLK_BYTES;   // 40 KB, a multiple of 1024
-constexpr int ACC_BUFS = 2;
-constexpr int TMEM_SF0 = ACC_BUFS * BN;       // scale columns after the two accumulators
-constexpr int SF_COLS_STAGE = 2 * MAX_BLK * 4;  // A and B blocks of one stage, 4 columns each
+constexpr int ACC_BUFS = 3;
+constexpr int TMEM_SF0 = ACC_BUFS * BN;       // scale columns after the accumulators
 constexpr int TMEM_COLS = 512;
 constexpr int EPI_WARP0 = 2;
-constexpr int EPI_WARPS = 4;
-constexpr int SF_WARP = EPI_WARP0 + EPI_WARPS;   // 6
-constexpr int SCHED_WARP = SF_WARP + 1;           // 7
+constexpr int EPI_GROUPS = 2;
+constexpr int EPI_WARPS = 4 * EPI_GROUPS;
+constexpr int SF_WARP = EPI_WARP0 + EPI_WARPS;    // 10
+constexpr int SCHED_WARP = SF_WARP + 1;           // 11
 constexpr int NUM_THREADS = 32 * (SCHED_WARP + 1);
 constexpr int SLOT = DMOE_SLOT_COLS;
 constexpr int TQ = 4;
 constexpr int HEAVY_MT = 3;
 constexpr int STG_BYTES = 32 * 64;
 static_assert(BN == SLOT, "one tile is one slot");
-static_assert(STAGE_BYTES % 1024 == 0, "stages keep the 1024-byte alignment of the swizzled boxes");
-static_assert(TMEM_SF0 + STAGES * SF_COLS_STAGE <= TMEM_COLS, "tensor memory");
+
+// Per-format layout: scale blocks per operand and stage (NVFP4: one per MMA),
+// stage bytes (operands, the two scale boxes, the blocks) and the stage count
+// that tensor memory allows next to the accumulators.
+template <int KIND>
+struct Layout {
+  static constexpr int NBLK = KIND == 0 ? 1 : 4;
+  static constexpr int OFF_B = A_BYTES;
+  static constexpr int OFF_SFA_BOX = A_BYTES + B_BYTES;
+  static constexpr int OFF_SFB_BOX = OFF_SFA_BOX + SFBOX_BYTES;
+  static constexpr int OFF_SFA_BLK = OFF_SFB_BOX + SFBOX_BYTES;
+  static constexpr int OFF_SFB_BLK = OFF_SFA_BLK + NBLK * SFBLK_BYTES;
+  static constexpr int STAGE_BYTES = ((OFF_SFB_BLK + NBLK * SFBLK_BYTES) + 1023) / 1024 * 1024;
+  static constexpr int SF_COLS_STAGE = 2 * NBLK * 4;     // A and B blocks of one stage, 4 columns each
+  static constexpr int STAGES = KIND == 0 ? 5 : 4;
+  static_assert(TMEM_SF0 + STAGES * SF_COLS_STAGE <= TMEM_COLS, "tensor memory");
+  static constexpr size_t SMEM = 1024 + size_t(STAGES) * STAGE_BYTES + size_t(EPI_WARPS) * STG_BYTES + 1024;
+  static_assert(SMEM <= 232448, "dynamic shared memory above the 227 KB a CTA may use");
+};
+constexpr int MAX_STAGES = 5;
 
 enum Kind : int { kMxf8 = 0, kNvf4 = 1 };
 
 struct alignas(16) Ctrl {
-  uint64_t full[STAGES];       // operand bytes landed
-  uint64_t sfin[STAGES];       // scale boxes landed
-  uint64_t sfrdy[STAGES];      // scale blocks written by the transposer
-  uint64_t empty[STAGES];      // the stage's MMAs and scale copies are done
+  uint64_t full[MAX_STAGES];   // operand bytes landed
+  uint64_t sfin[MAX_STAGES];   // scale boxes landed
+  uint64_t sfrdy[MAX_STAGES];  // scale blocks written by the transposer
+  uint64_t empty[MAX_STAGES];  // the stage's MMAs and scale copies are done
   uint64_t acc_full[ACC_BUFS];
   uint64_t acc_empty[ACC_BUFS];
   uint64_t mma_done;
@@ -105,8 +118,7 @@ struct alignas(16) Ctrl {
   int abort;
 };
 
-constexpr size_t kSmemBytes = 1024 + size_t(STAGES) * STAGE_BYTES + size_t(EPI_WARPS) * STG_BYTES + sizeof(Ctrl);
-static_assert(kSmemBytes <= 232448, "dynamic shared memory above the 227 KB a CTA may use");
+static_assert(sizeof(Ctrl) <= 1024, "control block");
 
 struct KParams {
   const int32_t* offsets;
@@ -186,9 +198,10 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
                        const __grid_constant__ CUtensorMap tmap_o, const KParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Ctrl& c = *reinterpret_cast<Ctrl*>(base + size_t(STAGES) * STAGE_BYTES + size_t(EPI_WARPS) * STG_BYTES);
+  using L = Layout<KIND>;
+  Ctrl& c = *reinterpret_cast<Ctrl*>(base + size_t(L::STAGES) * L::STAGE_BYTES + size_t(EPI_WARPS) * STG_BYTES);
   const uint32_t stage0 = smem_u32(base);
-  constexpr int NBLK = KIND == kMxf8 ? 1 : MAX_BLK;   // scale blocks per operand per stage
+  constexpr int NBLK = L::NBLK;   // scale blocks per operand per stage
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -196,7 +209,7 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
   const int E = p.E;
 
   if (tid == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < L::STAGES; ++s) {
       mbar_init(smem_u32(&c.full[s]), 1);
       mbar_init(smem_u32(&c.sfin[s]), 1);
       mbar_init(smem_u32(&c.sfrdy[s]), 1);
@@ -204,7 +217,7 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
     }
     for (int b = 0; b < ACC_BUFS; ++b) {
       mbar_init(smem_u32(&c.acc_full[b]), 1);
-      mbar_init(smem_u32(&c.acc_empty[b]), EPI_WARPS);
+      mbar_init(smem_u32(&c.acc_empty[b]), 4);   // the four warps of the group that took the tile
     }
     mbar_init(smem_u32(&c.mma_done), 1);
     for (int i = 0; i < TQ; ++i) {
@@ -247,25 +260,25 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
         bool ok = true;
         for (int kb = 0; kb < p.KB; ++kb) {
           if (!mbar_wait(smem_u32(&c.empty[stage]), ph ^ 1u, &c.abort, p.status, p.wait_ns)) { ok = false; break; }
-          const uint32_t sa = stage0 + stage * STAGE_BYTES;
+          const uint32_t sa = stage0 + stage * L::STAGE_BYTES;
           const uint32_t full = smem_u32(&c.full[stage]);
           const uint32_t sfin = smem_u32(&c.sfin[stage]);
           mbar_arrive_expect_tx(full, A_BYTES + B_BYTES);
           tma_load_2d(sa, &tmap_a, full, kb * ROWB, tl.row0);
-          tma_load_2d(sa + OFF_B, &tmap_b, full, kb * ROWB, brow);
+          tma_load_2d(sa + L::OFF_B, &tmap_b, full, kb * ROWB, brow);
           // 16 bytes of scales per row: four stages' words (MXFP8) or this stage's four (NVFP4)
           const int sx = KIND == kMxf8 ? 16 * (kb >> 2) : 16 * kb;
           mbar_arrive_expect_tx(sfin, 2 * SFBOX_BYTES);
-          tma_load_2d(sa + OFF_SFA_BOX, &tmap_sfa, sfin, sx, tl.row0);
-          tma_load_2d(sa + OFF_SFB_BOX, &tmap_sfb, sfin, sx, brow);
+          tma_load_2d(sa + L::OFF_SFA_BOX, &tmap_sfa, sfin, sx, tl.row0);
+          tma_load_2d(sa + L::OFF_SFB_BOX, &tmap_sfb, sfin, sx, brow);
           ++issued_total;
-          if (++stage == STAGES) { stage = 0; ph ^= 1u; }
+          if (++stage == L::STAGES) { stage = 0; ph ^= 1u; }
         }
         if (!ok) break;
       }
       // let every copy this thread started land before the CTA can exit
-      for (int s = 0; s < STAGES; ++s) {
-        const int n = (issued_total - s + STAGES - 1) / STAGES;
+      for (int s = 0; s < L::STAGES; ++s) {
+        const int n = (issued_total - s + L::STAGES - 1) / L::STAGES;
         if (n > 0) {
           mbar_wait_drain(smem_u32(&c.full[s]), uint32_t(n - 1) & 1u, p.wait_ns / 4);
           mbar_wait_drain(smem_u32(&c.sfin[s]), uint32_t(n - 1) & 1u, p.wait_ns / 4);
@@ -293,17 +306,17 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
           if (!mbar_wait(smem_u32(&c.full[stage]), ph, &c.abort, p.status, p.wait_ns)) { ok = false; break; }
           if (!mbar_wait(smem_u32(&c.sfrdy[stage]), ph, &c.abort, p.status, p.wait_ns)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t sa = stage0 + stage * STAGE_BYTES;
-          const uint32_t sf_a = tmem_base + uint32_t(TMEM_SF0 + stage * SF_COLS_STAGE);
-          const uint32_t sf_b = sf_a + uint32_t(MAX_BLK * 4);
+          const uint32_t sa = stage0 + stage * L::STAGE_BYTES;
+          const uint32_t sf_a = tmem_base + uint32_t(TMEM_SF0 + stage * L::SF_COLS_STAGE);
+          const uint32_t sf_b = sf_a + uint32_t(NBLK * 4);
           // scale blocks -> tensor memory (ordered before the MMAs this thread issues next)
 #pragma unroll
           for (int blk = 0; blk < NBLK; ++blk) {
-            tmem_cp_32x128b_x4(sf_a + uint32_t(4 * blk), smem_desc_sfblk(sa + OFF_SFA_BLK + blk * SFBLK_BYTES));
-            tmem_cp_32x128b_x4(sf_b + uint32_t(4 * blk), smem_desc_sfblk(sa + OFF_SFB_BLK + blk * SFBLK_BYTES));
+            tmem_cp_32x128b_x4(sf_a + uint32_t(4 * blk), smem_desc_sfblk(sa + L::OFF_SFA_BLK + blk * SFBLK_BYTES));
+            tmem_cp_32x128b_x4(sf_b + uint32_t(4 * blk), smem_desc_sfblk(sa + L::OFF_SFB_BLK + blk * SFBLK_BYTES));
           }
           const uint64_t adesc = smem_desc_k128(sa);
-          const uint64_t bdesc = smem_desc_k128(sa + OFF_B);
+          const uint64_t bdesc = smem_desc_k128(sa + L::OFF_B);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             // 32 bytes of each row per MMA: 32 E4M3 or 64 E2M1 values
@@ -313,7 +326,7 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
                          sf_a + 4 * blk, sf_b + 4 * blk, (kb | kk) != 0 ? 1u : 0u);
           }
           tc_commit(smem_u32(&c.empty[stage]));
-          if (++stage == STAGES) { stage = 0; ph ^= 1u; }
+          if (++stage == L::STAGES) { stage = 0; ph ^= 1u; }
         }
         if (!ok) break;
         tc_commit(smem_u32(&c.acc_full[acc]));
@@ -338,11 +351,11 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
       bool ok = true;
       for (int kb = 0; kb < p.KB; ++kb) {
         if (!warp_wait(smem_u32(&c.sfin[stage]), ph, &c.abort, p.status, lane, p.wait_ns)) { ok = false; break; }
-        const uint32_t sa = stage0 + stage * STAGE_BYTES;
+        const uint32_t sa = stage0 + stage * L::STAGE_BYTES;
 #pragma unroll
         for (int op = 0; op < 2; ++op) {
-          const uint32_t box = sa + (op == 0 ? OFF_SFA_BOX : OFF_SFB_BOX);
-          const uint32_t blk = sa + (op == 0 ? OFF_SFA_BLK : OFF_SFB_BLK);
+          const uint32_t box = sa + (op == 0 ? L::OFF_SFA_BOX : L::OFF_SFB_BOX);
+          const uint32_t blk = sa + (op == 0 ? L::OFF_SFA_BLK : L::OFF_SFB_BLK);
           uint4 r[4];
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc) r[cc] = lds_v4(box + uint32_t((32 * cc + lane) * 16));
@@ -366,7 +379,7 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
         fence_proxy_async_smem();   // the generic-proxy block writes, before the tensor core's copy reads them
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&c.sfrdy[stage]));
-        if (++stage == STAGES) { stage = 0; ph ^= 1u; }
+        if (++stage == L::STAGES) { stage = 0; ph ^= 1u; }
       }
       if (!ok) break;
     }
@@ -397,14 +410,17 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
       tile = __shfl_sync(0xffffffffu, nxt, 0);
     }
   } else {
-    // -------------------------------------------------- epilogue (4 warps)
-    // Warp w reads TMEM lanes 32*(w%4)..+31: 32 rows x the tile's 128 columns
-    // (one slot).  Same staging, stores and fixed in-slot tree as the bf16
-    // single-CTA kernel.
+    // -------------------------------------------------- epilogue (2 groups of 4 warps)
+    // Group g takes the CTA's tiles g, g+2, g+4, ...; tile i sits in
+    // accumulator i % 3.  Every epilogue warp reads every queue entry (to see
+    // the end marker).  Warp w reads TMEM lanes 32*(w%4)..+31: 32 rows x the
+    // tile's 128 columns (one slot).  Same staging, stores and fixed in-slot
+    // tree as the bf16 single-CTA kernel.
     const int q = warp & 3;
+    const int grp = (warp - EPI_WARP0) >> 2;
     const int k4 = lane & 3;
     const uint64_t pol_keep = policy_evict_last();
-    const uint32_t stg = stage0 + uint32_t(STAGES * STAGE_BYTES + (warp - EPI_WARP0) * STG_BYTES);
+    const uint32_t stg = stage0 + uint32_t(L::STAGES * L::STAGE_BYTES + (warp - EPI_WARP0) * STG_BYTES);
     float alpha = 1.0f;
     if (KIND == kNvf4) alpha = __frcp_rn(__fmul_rn(__ldg(p.s_enc_x), __ldg(p.s_enc_w)));
     int acc = 0;
@@ -417,6 +433,10 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&c.tq_empty[qs]));
       if (cur < 0) break;
+      if ((qi & 1) != grp) {
+        if (++acc == ACC_BUFS) { acc = 0; aph ^= 1u; }
+        continue;
+      }
       const int col0 = tl.n0;
       int rr[4], src[4];
       bool ok[4];
@@ -531,10 +551,11 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
 
 template <int KIND, int MODE>
 cudaError_t launch_kind_mode(const CUtensorMap* maps, const KParams& kp, int grid, cudaStream_t stream) {
+  using L = Layout<KIND>;
   const cudaError_t e =
-      ensure_kernel_smem(reinterpret_cast<const void*>(grouped_gemm_bs_kernel<KIND, MODE>), int(kSmemBytes));
+      ensure_kernel_smem(reinterpret_cast<const void*>(grouped_gemm_bs_kernel<KIND, MODE>), int(L::SMEM));
   if (e != cudaSuccess) return e;
-  return launch_chained(grouped_gemm_bs_kernel<KIND, MODE>, dim3(grid), dim3(NUM_THREADS), kSmemBytes, stream,
+  return launch_chained(grouped_gemm_bs_kernel<KIND, MODE>, dim3(grid), dim3(NUM_THREADS), L::SMEM, stream,
                         maps[0], maps[1], maps[2], maps[3], maps[4], kp);
 }
 

@@ -212,3 +212,23 @@ def test_block_scaled_rejects_unsupported_shapes():
         api.grouped_gemm_dprob_mxfp8(x, xs, w, wsc, prob.off, prob.G, prob.src, cfg.topk, prob.ws)
     assert ei.value.status == 2
     del enc
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_block_scaled_dprob_is_the_combine_of_its_slots(kind):
+    """dprob of the block-scaled call is bit for bit the fixed-order combine
+    of the slots it returns, written afresh on every call (NaN-filled
+    buffers) and for every grid size."""
+    cfg = SHAPES[1]
+    prob = Problem(cfg)
+    enc = Encoded(prob, kind)
+    nan = lambda: torch.full((cfg.T, cfg.topk), float("nan"), device="cuda")
+    out, dprob, slots = enc.run(prob, dprob=nan())
+    assert api.read_status(prob.ws) == 0
+    ref = api.dprob_combine(slots, prob.src, cfg.topk, dprob=nan())
+    assert not torch.isnan(ref).any()
+    assert torch.equal(dprob.view(torch.int32), ref.view(torch.int32))
+    for num_ctas in (0, 9, 1):
+        _, d, _ = enc.run(prob, num_ctas=num_ctas, dprob=nan())
+        assert api.read_status(prob.ws) == 0
+        assert torch.equal(d.view(torch.int32), ref.view(torch.int32))
