@@ -359,7 +359,7 @@ def block_scaled_measure(api, cfg, X, W, G, off, src, ws, timed, iters):
                      "peak_source": f"measured bf16 burst x {ratio:g} (nominal dense ratio)",
                      "tensor_frac": tf / peak, "algorithmic_bytes": b, "achieved_gbs": b / (ms * 1e-3) / 1e9,
                      "hbm_frac": b / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
-                     "kernel": "grouped_gemm_bs_kernel (128x128 tiles, single CTA)"}
+                     "kernel": "grouped_gemm_bs_kernel (128x128 tiles, one CTA per SM, two epilogue groups, three accumulators)"}
         del xq, xs, wq, wsc
     del out, sl, dp
     torch.cuda.empty_cache()

@@ -110,6 +110,7 @@ SHAPES = [
     synth.custom_config("bs_ragged", T=500, E=12, topk=3, K=1024, N=384, index=402),
     synth.custom_config("bs_manyexp", T=400, E=64, topk=4, K=512, N=256, index=403),
     synth.custom_config("bs_zipf", T=600, E=16, topk=4, K=512, N=512, routing="zipf", index=404),
+    synth.custom_config("bs_n128", T=300, E=5, topk=2, K=512, N=128, index=406),     # one slot, one n-tile
 ]
 
 
@@ -232,3 +233,16 @@ def test_block_scaled_dprob_is_the_combine_of_its_slots(kind):
         _, d, _ = enc.run(prob, num_ctas=num_ctas, dprob=nan())
         assert api.read_status(prob.ws) == 0
         assert torch.equal(d.view(torch.int32), ref.view(torch.int32))
+
+
+def test_nvfp4_single_stage_k256():
+    """NVFP4 at its smallest K (256: one 128-byte stage per row, one 16-byte
+    scale unit), ragged experts, every row against the oracle."""
+    cfg = synth.custom_config("bs_k256", T=400, E=7, topk=3, K=256, N=256, index=407)
+    prob = Problem(cfg)
+    enc = Encoded(prob, "nvfp4")
+    out, dprob, slots = enc.run(prob)
+    assert api.read_status(prob.ws) == 0
+    rows = np.arange(cfg.R)
+    Y, Yb, P, D, src = oracle_rows(prob, "nvfp4", rows, check_codes=enc)
+    gpu_util.compare_rows(out, slots, dprob, rows, Y, Yb, P, D, src, prob.inp.G, cfg.topk)
