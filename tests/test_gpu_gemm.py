@@ -55,6 +55,35 @@ def test_full_parity_small_shapes(cfg, flags):
     gpu_util.check_rows_against_oracle(prob, out, slots, dprob, rows)
 
 
+def fuzz_shapes(n, seed=2024):
+    """Seeded random shapes inside the supported envelope: T 50-900 tokens,
+    1-96 experts, top-1 to top-8, K a multiple of 8 up to 1024, N a multiple
+    of 128 up to 1024, uniform or Zipf routing."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        E = int(rng.integers(1, 97))
+        topk = int(rng.integers(1, min(8, E) + 1))
+        T = int(rng.integers(50, 901))
+        K = 8 * int(rng.integers(1, 129))
+        N = 128 * int(rng.integers(1, 9))
+        routing = "zipf" if rng.random() < 0.5 else "uniform"
+        out.append(synth.custom_config(f"fuzz{i}", T=T, E=E, topk=topk, K=K, N=N, routing=routing, index=320 + i))
+    return out
+
+
+FUZZ = fuzz_shapes(8)
+
+
+@pytest.mark.parametrize("flags", KERNELS, ids=KERNEL_IDS)
+@pytest.mark.parametrize("cfg", FUZZ, ids=[f"{c.name}-T{c.T}-E{c.E}-k{c.topk}-K{c.K}-N{c.N}" for c in FUZZ])
+def test_fuzz_shapes_full_parity(cfg, flags):
+    prob = Problem(cfg)
+    out, dprob, slots = prob.run_dprob(flags=flags)
+    assert api.read_status(prob.ws) == 0
+    gpu_util.check_rows_against_oracle(prob, out, slots, dprob, np.arange(cfg.R))
+
+
 @pytest.mark.parametrize("flags", KERNELS, ids=KERNEL_IDS)
 @pytest.mark.parametrize("cfg", SHAPES[:2], ids=[c.name for c in SHAPES[:2]])
 def test_fwd_equals_dprob_output_and_unfused_epilogue(cfg, flags):
