@@ -65,7 +65,8 @@ constexpr int ROWB = 128;                     // operand bytes per row per stage
 constexpr int A_BYTES = BM * ROWB;            // 16 KB
 constexpr int B_BYTES = BN * ROWB;            // 16 KB
 constexpr int SFBOX_BYTES = 128 * 16;         // TMA box of scale bytes: 128 rows x 16 bytes
-constexpr int SFBLK_BYTES = 32 * 16;          // one tcgen05.cp block: 32 rows x 16 bytes
+constexpr int SFBLK_BYTES = 32 * 16;          // one .32x128b tcgen05.cp source: 32 rows x 16 bytes
+constexpr int SF256_BYTES = 128 * 32;         // one .128x256b tcgen05.cp source: 128 rows x 32 bytes
 constexpr int ACC_BUFS = 3;
 constexpr int TMEM_SF0 = ACC_BUFS * BN;       // scale columns after the accumulators
 constexpr int TMEM_COLS = 512;
@@ -81,19 +82,26 @@ constexpr int HEAVY_MT = 3;
 constexpr int STG_BYTES = 32 * 64;
 static_assert(BN == SLOT, "one tile is one slot");
 
-// Per-format layout: scale blocks per operand and stage (NVFP4: one per MMA),
-// stage bytes (operands, the two scale boxes, the blocks) and the stage count
-// that tensor memory allows next to the accumulators.
+// Per-format layout: stage bytes (operands, the two scale boxes, the
+// scale sources of the tensor-memory copies), the scale columns a stage
+// takes in tensor memory, and the stage count that shared and tensor memory
+// allow next to the accumulators.
+//   MXFP8: one 32-row x 16-byte block per operand (one .32x128b.warpx4 copy
+//          each, 4 columns; the four MMAs take the four bytes of a word).
+//   NVFP4: two 128-row x 32-byte sources per operand (four .128x256b copies,
+//          8 columns each; every MMA takes a whole word): 32 columns.  An
+//          MMA's scale address must sit on a multiple of 4 columns, so the
+//          four MMAs of a stage read A at columns 4 kk and B at 16 + 4 kk.
 template <int KIND>
 struct Layout {
-  static constexpr int NBLK = KIND == 0 ? 1 : 4;
   static constexpr int OFF_B = A_BYTES;
   static constexpr int OFF_SFA_BOX = A_BYTES + B_BYTES;
   static constexpr int OFF_SFB_BOX = OFF_SFA_BOX + SFBOX_BYTES;
   static constexpr int OFF_SFA_BLK = OFF_SFB_BOX + SFBOX_BYTES;
-  static constexpr int OFF_SFB_BLK = OFF_SFA_BLK + NBLK * SFBLK_BYTES;
-  static constexpr int STAGE_BYTES = ((OFF_SFB_BLK + NBLK * SFBLK_BYTES) + 1023) / 1024 * 1024;
-  static constexpr int SF_COLS_STAGE = 2 * NBLK * 4;     // A and B blocks of one stage, 4 columns each
+  static constexpr int SRC_BYTES = KIND == 0 ? SFBLK_BYTES : SF256_BYTES;
+  static constexpr int OFF_SFB_BLK = OFF_SFA_BLK + (KIND == 0 ? 1 : 2) * SRC_BYTES;
+  static constexpr int STAGE_BYTES = ((OFF_SFB_BLK + (KIND == 0 ? 1 : 2) * SRC_BYTES) + 1023) / 1024 * 1024;
+  static constexpr int SF_COLS_STAGE = KIND == 0 ? 8 : 32;
   static constexpr int STAGES = KIND == 0 ? 5 : 4;
   static_assert(TMEM_SF0 + STAGES * SF_COLS_STAGE <= TMEM_COLS, "tensor memory");
   static constexpr size_t SMEM = 1024 + size_t(STAGES) * STAGE_BYTES + size_t(EPI_WARPS) * STG_BYTES + 1024;
@@ -156,6 +164,27 @@ __device__ __forceinline__ uint64_t smem_desc_sfblk(uint32_t saddr) {
   return d;
 }
 
+// A 128-row x 32-byte source for tcgen05.cp .128x256b: no swizzle, 8-row x
+// 16-byte core matrices; the two 16-byte halves of a row group 128 bytes
+// apart (leading byte offset), row groups 256 bytes apart (stride byte offset).
+__device__ __forceinline__ uint64_t smem_desc_sf256(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= uint64_t((saddr & 0x3FFFFu) >> 4);
+  d |= uint64_t(128 >> 4) << 16;
+  d |= uint64_t(256 >> 4) << 32;
+  d |= uint64_t(1) << 46;
+  return d;
+}
+
+// Byte offset of 32-bit word slot s (0..7) of row r in such a source.
+__device__ __forceinline__ uint32_t sf256_word(int r, int s) {
+  return uint32_t((r >> 3) * 256 + (s >> 2) * 128 + (r & 7) * 16 + (s & 3) * 4);
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {   // i is a compile-time constant
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
 // Instruction descriptor of the block-scaled kinds: B scale id (bits 4-5),
 // A and B formats (7-9, 10-12), both K-major, N >> 3 (17-22), scale format
 // (23: 1 = E8M0, 0 = E4M3), M >> 4 (24-28), A scale id (29-30).
@@ -185,6 +214,12 @@ __device__ __forceinline__ void bs_mma(uint32_t d_tmem, uint64_t a_desc, uint64_
   }
 }
 
+// 128 rows x 256 bits of shared memory into tensor-memory lanes 0..127 (row
+// r to lane r), 8 columns from taddr.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // 32 rows x 128 bits of shared memory into tensor-memory lanes 32w + j of
 // the 4 columns at taddr, for each lane quarter w.
 __device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
@@ -201,7 +236,6 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
   using L = Layout<KIND>;
   Ctrl& c = *reinterpret_cast<Ctrl*>(base + size_t(L::STAGES) * L::STAGE_BYTES + size_t(EPI_WARPS) * STG_BYTES);
   const uint32_t stage0 = smem_u32(base);
-  constexpr int NBLK = L::NBLK;   // scale blocks per operand per stage
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -307,23 +341,30 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
           if (!mbar_wait(smem_u32(&c.sfrdy[stage]), ph, &c.abort, p.status, p.wait_ns)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = stage0 + stage * L::STAGE_BYTES;
-          const uint32_t sf_a = tmem_base + uint32_t(TMEM_SF0 + stage * L::SF_COLS_STAGE);
-          const uint32_t sf_b = sf_a + uint32_t(NBLK * 4);
-          // scale blocks -> tensor memory (ordered before the MMAs this thread issues next)
-#pragma unroll
-          for (int blk = 0; blk < NBLK; ++blk) {
-            tmem_cp_32x128b_x4(sf_a + uint32_t(4 * blk), smem_desc_sfblk(sa + L::OFF_SFA_BLK + blk * SFBLK_BYTES));
-            tmem_cp_32x128b_x4(sf_b + uint32_t(4 * blk), smem_desc_sfblk(sa + L::OFF_SFB_BLK + blk * SFBLK_BYTES));
+          const uint32_t sfc = tmem_base + uint32_t(TMEM_SF0 + stage * L::SF_COLS_STAGE);
+          // scale sources -> tensor memory (ordered before the MMAs this thread issues next)
+          if (KIND == kMxf8) {
+            tmem_cp_32x128b_x4(sfc, smem_desc_sfblk(sa + L::OFF_SFA_BLK));
+            tmem_cp_32x128b_x4(sfc + 4u, smem_desc_sfblk(sa + L::OFF_SFB_BLK));
+          } else {
+            tmem_cp_128x256b(sfc, smem_desc_sf256(sa + L::OFF_SFA_BLK));
+            tmem_cp_128x256b(sfc + 8u, smem_desc_sf256(sa + L::OFF_SFA_BLK + SF256_BYTES));
+            tmem_cp_128x256b(sfc + 16u, smem_desc_sf256(sa + L::OFF_SFB_BLK));
+            tmem_cp_128x256b(sfc + 24u, smem_desc_sf256(sa + L::OFF_SFB_BLK + SF256_BYTES));
           }
           const uint64_t adesc = smem_desc_k128(sa);
           const uint64_t bdesc = smem_desc_k128(sa + L::OFF_B);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            // 32 bytes of each row per MMA: 32 E4M3 or 64 E2M1 values
-            const uint32_t blk = KIND == kMxf8 ? 0u : uint32_t(kk);
+            // 32 bytes of each row per MMA: 32 E4M3 or 64 E2M1 values.  MXFP8:
+            // byte kk of the stage's word (scale id); NVFP4: the word of MMA kk,
+            // for tile row 32c + j at column 4 kk + c (A) or 16 + 4 kk + c (B)
+            // of the stage's scale columns
             const uint32_t sfid = KIND == kMxf8 ? uint32_t(kk) : 0u;
-            bs_mma<KIND>(d_tmem, adesc + uint64_t(kk * 2), bdesc + uint64_t(kk * 2), bs_idesc<KIND>(sfid),
-                         sf_a + 4 * blk, sf_b + 4 * blk, (kb | kk) != 0 ? 1u : 0u);
+            const uint32_t sfa = KIND == kMxf8 ? sfc : sfc + 4u * uint32_t(kk);
+            const uint32_t sfb = KIND == kMxf8 ? sfc + 4u : sfc + 16u + 4u * uint32_t(kk);
+            bs_mma<KIND>(d_tmem, adesc + uint64_t(kk * 2), bdesc + uint64_t(kk * 2), bs_idesc<KIND>(sfid), sfa, sfb,
+                         (kb | kk) != 0 ? 1u : 0u);
           }
           tc_commit(smem_u32(&c.empty[stage]));
           if (++stage == L::STAGES) { stage = 0; ph ^= 1u; }
@@ -337,8 +378,15 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
     }
   } else if (warp == SF_WARP) {
     // -------------------------------------------------- scale transposer
-    // box row t holds the 16 scale bytes of tile row t (four 32-bit words);
-    // block word (j, c) = the wanted word of tile row 32c + j, lane j writing row j
+    // Box row t holds the 16 scale bytes of tile row t (four 32-bit words).
+    // MXFP8: block word (j, c) = this stage's word of tile row 32c + j, lane j
+    //        writing block row j (one .32x128b.warpx4 copy per operand).
+    // NVFP4: source h (of each operand) holds, in every 32-row quarter q,
+    //        row 32q + j = at slot 4k' + c the word of MMA 2h + k' of tile row
+    //        32c + j, so tensor-memory lane 32q + j, column 8h + 4k' + c holds
+    //        the scale of tile row 32c + j for that MMA in every lane quarter,
+    //        as the replicating .32x128b.warpx4 copy lays it out.  Lane j owns
+    //        tile rows j, 32 + j, 64 + j, 96 + j.
     int stage = 0;
     uint32_t ph = 0;
     for (int qi = 0;; ++qi) {
@@ -369,11 +417,16 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
             o.w = w == 0 ? r[3].x : w == 1 ? r[3].y : w == 2 ? r[3].z : r[3].w;
             sts_v4(blk + uint32_t(lane * 16), o);
           } else {
-            // block kk (MMA kk) takes word kk of every row
-            sts_v4(blk + uint32_t(0 * SFBLK_BYTES + lane * 16), make_uint4(r[0].x, r[1].x, r[2].x, r[3].x));
-            sts_v4(blk + uint32_t(1 * SFBLK_BYTES + lane * 16), make_uint4(r[0].y, r[1].y, r[2].y, r[3].y));
-            sts_v4(blk + uint32_t(2 * SFBLK_BYTES + lane * 16), make_uint4(r[0].z, r[1].z, r[2].z, r[3].z));
-            sts_v4(blk + uint32_t(3 * SFBLK_BYTES + lane * 16), make_uint4(r[0].w, r[1].w, r[2].w, r[3].w));
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int k2 = 0; k2 < 2; ++k2) {
+                const int kk = 2 * h + k2;
+                const uint4 o = make_uint4(word_of(r[0], kk), word_of(r[1], kk), word_of(r[2], kk), word_of(r[3], kk));
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq)
+                  sts_v4(blk + uint32_t(h * SF256_BYTES) + sf256_word(32 * qq + lane, 4 * k2), o);
+              }
           }
         }
         fence_proxy_async_smem();   // the generic-proxy block writes, before the tensor core's copy reads them
