@@ -805,6 +805,46 @@ def run_ours(args):
     return 0
 
 
+def combine_only(args):
+    """The fixed-order slot combine alone, on the slot buffer of --config
+    (S x R fp32, seeded normal values, a seeded random permutation as
+    row_src): 3 warm-up launches, then 5 launches each after an L2 flush.
+    Prints one JSON object; not part of the bench line (a short command for
+    an ncu capture of this one kernel)."""
+    import torch
+    from bitwise_deterministic_moe_gb300 import api, build
+    build.build()
+    api.load()
+    dev = torch.device("cuda", 0)
+    cfg = synth.CONFIGS[args.config]
+    gen = torch.Generator(device=dev).manual_seed(cfg.seed)
+    sl = torch.randn(cfg.S, cfg.R, device=dev, generator=gen)
+    src = torch.randperm(cfg.R, device=dev, generator=gen).to(torch.int32)
+    dp = torch.empty(cfg.T, cfg.topk, dtype=torch.float32, device=dev)
+    l2_bytes = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or (128 << 20))
+    flush_buf = torch.empty(2 * l2_bytes // 4, dtype=torch.int32, device=dev)
+    flush_rd = torch.ones(2 * l2_bytes // 4, dtype=torch.int32, device=dev)
+    flush_sink = torch.empty((), dtype=torch.int64, device=dev)
+    for _ in range(3):
+        api.dprob_combine(sl, src, cfg.topk, dprob=dp)
+    t = []
+    for _ in range(5):
+        flush_buf.fill_(1)
+        torch.sum(flush_rd, dim=0, out=flush_sink)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        api.dprob_combine(sl, src, cfg.topk, dprob=dp)
+        b.record()
+        torch.cuda.synchronize(dev)
+        t.append(a.elapsed_time(b))
+    pk, _ = peaks()
+    b = cfg.S * cfg.R * 4 + 2 * cfg.R * 4
+    ms = float(np.median(t))
+    print(json.dumps({"pass": "slot_combine", "config": cfg.name, "rows": cfg.R, "slots": cfg.S,
+                      "algorithmic_bytes": b, "ms": ms, "frac": b / (ms * 1e-3) / 1e9 / pk["hbm_gbs"]}))
+    return 0
+
+
 def dense_compare(args):
     """The grouped GEMM on dense shapes (one expert holding every row, or equal
     experts) next to cuBLAS (torch.matmul / torch.bmm) on the same bf16
@@ -882,9 +922,13 @@ def main():
                     help="GEMM kernel: the call's own choice, or force one (same bits)")
     ap.add_argument("--dense-compare", action="store_true",
                     help="time the grouped GEMM on dense shapes next to cuBLAS and exit")
+    ap.add_argument("--combine-only", action="store_true",
+                    help="time the slot combine alone on --config's buffer sizes and exit")
     args = ap.parse_args()
     if args.dense_compare:
         return dense_compare(args)
+    if args.combine_only:
+        return combine_only(args)
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     if args.impl == "reference":
