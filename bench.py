@@ -437,6 +437,9 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     api.load()
+    # keep grad_out resident in L2 for the dprob epilogue's gathers: a context
+    # setting made once, before any timed work (--no-l2-reserve leaves it unset)
+    l2_reserved = api.reserve_l2_persisting(0 if args.no_l2_reserve else cfg.T * cfg.N * 2)
 
     def bf16(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
@@ -557,6 +560,12 @@ def run_ours(args):
 
     call_cold = timed_each(gemm_call, args.call_runs, True)
     call_hot = timed_each(gemm_call, args.call_runs, False)
+    call_unreserved = None
+    if l2_reserved:
+        # the same call with no persisting-L2 set-aside, for comparison
+        api.reserve_l2_persisting(0)
+        call_unreserved = timed_each(gemm_call, args.call_runs, False)
+        api.reserve_l2_persisting(l2_reserved)
     if api.read_status(ws) != 0:
         raise RuntimeError("device status set while timing single calls")
 
@@ -773,6 +782,9 @@ def run_ours(args):
                  # flush (cold) and back to back (hot)
                  "call_l2_flushed": dict(call_cold, tflops=flops / (call_cold["median_ms"] * 1e-3) / 1e12),
                  "call_l2_hot": dict(call_hot, tflops=flops / (call_hot["median_ms"] * 1e-3) / 1e12)})
+    if call_unreserved is not None:
+        roof["call_l2_hot_no_l2_reserve"] = dict(call_unreserved,
+                                                 tflops=flops / (call_unreserved["median_ms"] * 1e-3) / 1e12)
     line = {
         "metric": "grouped-GEMM+dprob TFLOP/s", "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -784,7 +796,8 @@ def run_ours(args):
                                                                             + cfg.T * cfg.N) * 2 / 1e9),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "maxvio": synth.maxvio(inp.topk_ids, cfg.E),
-                   "gemm_launch": {"kernel": gemm_kernel, "num_ctas": args.num_ctas or "all resident"}},
+                   "gemm_launch": {"kernel": gemm_kernel, "num_ctas": args.num_ctas or "all resident"},
+                   "l2_persisting_bytes": l2_reserved},
         "gpu_launches": launches_per_step * args.steps,
         "roofline": roof,
         "determinism_tax": tax,
@@ -917,6 +930,8 @@ def main():
     ap.add_argument("--skip-wgrad", action="store_true")
     ap.add_argument("--skip-quant", action="store_true")
     ap.add_argument("--skip-block-scaled", action="store_true")
+    ap.add_argument("--no-l2-reserve", action="store_true",
+                    help="do not set aside persisting L2 for grad_out (dmoe_reserve_l2_persisting)")
     ap.add_argument("--num-ctas", type=int, default=0, help="persistent CTAs of the GEMM (0 = all resident)")
     ap.add_argument("--kernel", default="auto", choices=sorted(KERNEL_FLAGS),
                     help="GEMM kernel: the call's own choice, or force one (same bits)")

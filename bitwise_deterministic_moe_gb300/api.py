@@ -72,6 +72,7 @@ def load() -> ctypes.CDLL:
         "dmoe_version": ([], I),
         "dmoe_workspace_bytes": ([I, I, I], SZ),
         "dmoe_read_status": ([P, P], I),
+        "dmoe_reserve_l2_persisting": ([SZ, ctypes.POINTER(ctypes.c_size_t)], I),
         "dmoe_permute_indices": ([P, I, I, I, P, P, P, P, SZ, P], I),
         "moe_dispatch_gather": ([P, P, I, I, I, P, P, SZ, P], I),
         "moe_token_combine": ([P, P, P, I, I, I, P, P, SZ, P], I),
@@ -135,6 +136,17 @@ def workspace(T: int, topk: int, E: int, device=None) -> torch.Tensor:
     """Zero-filled device workspace for a problem of this size."""
     n = workspace_bytes(T, topk, E)
     return torch.zeros(n, dtype=torch.uint8, device=device or torch.cuda.current_device())
+
+
+def reserve_l2_persisting(nbytes: int) -> int:
+    """Sets the context's persisting-L2 set-aside that keeps grad_out
+    resident for the dprob epilogue (clamped to half of L2 and the device
+    maximum; 0 releases it).  Returns the bytes in effect."""
+    if nbytes < 0:
+        raise ValueError("nbytes must be >= 0")
+    got = ctypes.c_size_t(0)
+    _check(load().dmoe_reserve_l2_persisting(int(nbytes), ctypes.byref(got)), "dmoe_reserve_l2_persisting")
+    return int(got.value)
 
 
 def read_status(ws: torch.Tensor, stream=None) -> int:

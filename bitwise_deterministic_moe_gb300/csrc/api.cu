@@ -161,6 +161,28 @@ dmoe_status dmoe_read_status(void* ws, dmoe_stream_t stream) {
   return static_cast<dmoe_status>(v);
 }
 
+dmoe_status dmoe_reserve_l2_persisting(size_t bytes, size_t* granted) {
+  int dev = 0, max_persist = 0, l2 = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&max_persist, cudaDevAttrMaxPersistingL2CacheSize, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return DMOE_ERR_CUDA;
+  }
+  // at most half of L2: a larger set-aside starves the streamed operands
+  size_t cap = size_t(l2) / 2;
+  if (size_t(max_persist) < cap) cap = size_t(max_persist);
+  const size_t want = bytes < cap ? bytes : cap;
+  size_t now = 0;
+  if (cudaDeviceSetLimit(cudaLimitPersistingL2CacheSize, want) != cudaSuccess ||
+      cudaDeviceGetLimit(&now, cudaLimitPersistingL2CacheSize) != cudaSuccess) {
+    cudaGetLastError();
+    return DMOE_ERR_CUDA;
+  }
+  if (granted) *granted = now;
+  return DMOE_OK;
+}
+
 dmoe_status dmoe_permute_indices(const int32_t* topk_ids, int T, int topk, int E, int32_t* expert_offsets,
                                  int32_t* row_src, int32_t* row_of, void* ws, size_t ws_bytes,
                                  dmoe_stream_t stream) {

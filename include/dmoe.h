@@ -213,6 +213,25 @@ dmoe_status moe_grouped_gemm_dprob(const void* X_perm, const void* W, const int3
                                    dmoe_stream_t stream);
 
 /*
+ * L2 residency of grad_out for the dprob epilogue.  Every grad_out row is
+ * gathered by topk different tiles at different times while the weights and
+ * expert_out stream through L2; the epilogue loads it with an L2 evict-last
+ * policy, and such lines are kept resident only inside the context's
+ * persisting-L2 set-aside, which is empty unless the process sets one.  This
+ * host call sets it (cudaLimitPersistingL2CacheSize of the current device's
+ * context) to `bytes` clamped to [0, min(the device maximum, L2 size / 2)]
+ * and writes the value then in effect to *granted (may be null; the runtime
+ * may round the request up to its own granularity).  Size it to
+ * grad_out (T*N*2 bytes) once, before the calls; 0 releases it.  It is a
+ * context-wide setting: it also takes up to that much L2 away from the
+ * normal accesses of every other kernel of the process, and it ends with the
+ * context.  No other call of this library changes it.  Results never depend
+ * on it, only timing.  May synchronize the device.  DMOE_ERR_CUDA if a
+ * runtime query or the setting is refused.
+ */
+dmoe_status dmoe_reserve_l2_persisting(size_t bytes, size_t* granted);
+
+/*
  * The nondeterministic control (the original form the pages describe): the
  * same GEMM and per-slot partials, but every partial is added with an fp32
  * atomicAdd into dprob[row_src[r]] after the call zero-fills dprob on

@@ -281,3 +281,29 @@ def test_combine_vector_and_general_forms(R, S, aligned):
     want[src_h.numpy()] = acc
     got = dprob.reshape(-1).cpu().numpy()
     assert np.array_equal(got.view(np.int32), want.view(np.int32))
+
+
+@pytest.mark.parametrize("name", ["latent", "imbal"])
+def test_l2_reserve_changes_timing_only(name):
+    """With grad_out's persisting-L2 set-aside in place (the setting the
+    benchmark makes), the call's expert_out, slots and dprob equal the ones
+    without it bit for bit; the set-aside is clamped to half of L2 and 0
+    releases it."""
+    prob = Problem(synth.CONFIGS[name])
+    assert api.reserve_l2_persisting(0) == 0
+    o1, d1, s1 = prob.run_dprob()
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    want = min(prob.cfg.T * prob.cfg.N * 2, l2 // 2)
+    slack = 4 << 20                        # the runtime rounds to its own granularity
+    got = api.reserve_l2_persisting(prob.cfg.T * prob.cfg.N * 2)
+    try:
+        assert abs(got - want) <= slack
+        assert api.reserve_l2_persisting(1 << 40) <= l2 // 2 + slack
+        api.reserve_l2_persisting(got)
+        o2, d2, s2 = prob.run_dprob()
+        assert api.read_status(prob.ws) == 0
+    finally:
+        assert api.reserve_l2_persisting(0) == 0
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(s1.view(torch.int32), s2.view(torch.int32))
+    assert torch.equal(d1.view(torch.int32), d2.view(torch.int32))
