@@ -463,13 +463,25 @@ def run_ours(args):
     fp_src = torch.empty(api.fingerprint_num_chunks(R * 4), dtype=torch.int64, device=dev)
     fp_dp = torch.empty(api.fingerprint_num_chunks(R * 4), dtype=torch.int64, device=dev)
     stream = torch.cuda.current_stream(dev)
-    # routing 3 (histogram, block scan with offsets, scatter), fingerprint 1,
-    # GEMM + slot combine 2, fingerprint 1
-    launches_per_step = 3 + 1 + 2 + 1
+    # routing 3 (histogram, block scan with offsets, scatter), GEMM 1, slot
+    # combine taking the row_src and dprob fingerprints 1 (--separate-fp:
+    # fingerprint 1 before the GEMM call and 1 after it instead)
+    launches_per_step = 3 + 1 + 2 + 1 if args.separate_fp else 3 + 2
 
     def step(ev=None, inputs=None):
         ids_, X_, G_ = inputs if inputs is not None else (ids, X, G)
         api.permute_indices(ids_, cfg.E, ws, off, src, row_of=row_of)
+        if not args.separate_fp:
+            # the deterministic call whose combine also takes the chunk
+            # fingerprints of row_src (the routing map) and dprob
+            if ev is not None:
+                ev[0].record(stream)
+            api.grouped_gemm_dprob_fp(X_, W, off, G_, src, k, ws, out=out, slots=slots, dprob=dprob,
+                                      row_src_hash=fp_src, dprob_hash=fp_dp,
+                                      num_ctas=args.num_ctas, flags=KERNEL_FLAGS[args.kernel])
+            if ev is not None:
+                ev[1].record(stream)
+            return
         api.fingerprint(src, out=fp_src)
         if ev is not None:
             ev[0].record(stream)
@@ -489,8 +501,12 @@ def run_ours(args):
     flops, abytes = algorithmic(cfg, off_np)
 
     # ---------------- timed region: K steps, inputs resident in HBM (> L2)
+    # The GEMM call is bracketed by events on every EV_EVERY-th step only: an
+    # event between two programmatically chained launches exposes the next
+    # launch's latency (~6 us a step with events on every step).
+    ev_every = max(1, min(4, args.steps // 3))
     gemm_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
+               if i % ev_every == 0 else None for i in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local)
@@ -508,7 +524,8 @@ def run_ours(args):
         dist.barrier()
     clocks = sampler.stop()
     ms = t_start.elapsed_time(t_end)
-    gemm_ms = float(np.mean([a.elapsed_time(b) for a, b in gemm_ev]))
+    gemm_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in gemm_ev if e is not None]))
+    gemm_calls_timed = sum(e is not None for e in gemm_ev)
     if api.read_status(ws) != 0:
         raise RuntimeError("device status set during the timed region")
     ms_max = max_over_ranks(ms, world)
@@ -768,7 +785,11 @@ def run_ours(args):
     pairs = args.kernel == "pairs" or (args.kernel == "auto" and cfg.R >= 512 * cfg.E)
     gemm_kernel = "grouped_gemm_pair_kernel<slots>" if pairs else "grouped_gemm_kernel<slots>"
     roof.update({"kernel": gemm_kernel + " + combine (moe_grouped_gemm_dprob)",
-                 "launch_ms": gemm_ms, "algorithmic_bytes": abytes, "algorithmic_flops": flops,
+                 "launch_ms": gemm_ms, "launch_ms_calls": f"{gemm_calls_timed} of the {args.steps} timed calls (one in every {ev_every} steps)",
+                 "launch_call": "moe_grouped_gemm_dprob" if args.separate_fp else
+                                "moe_grouped_gemm_dprob_fp (the same call, its combine also fingerprinting row_src and dprob)",
+                 "single_call_runs": "moe_grouped_gemm_dprob (call_l2_flushed, call_l2_hot)",
+                 "algorithmic_bytes": abytes, "algorithmic_flops": flops,
                  "peak_source": f"{pk_kind} ({PEAKS_FILE if pk_kind == 'measured' else 'profiling recipe'})",
                  "tensor_frac": achieved_tf / tc_peak, "tensor_tflops": achieved_tf,
                  "tensor_peak": {"tflops": tc_peak, "kind": peak_kind,
@@ -791,7 +812,9 @@ def run_ours(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"{cfg.name}: T={cfg.T} E={cfg.E} topk={cfg.topk} K={cfg.K} N={cfg.N} "
                                f"routing={cfg.routing} (seed {cfg.seed})",
-                   "step": "permute + fingerprint(row_src) + grouped GEMM/slot dprob/combine + fingerprint(dprob)",
+                   "step": ("permute + grouped GEMM/slot dprob/combine, the combine also fingerprinting row_src and dprob"
+                            if not args.separate_fp else
+                            "permute + fingerprint(row_src) + grouped GEMM/slot dprob/combine + fingerprint(dprob)"),
                    "l2": "inputs larger than L2 (X+W+grad_out = %.2f GB)" % ((cfg.R * cfg.K + cfg.E * cfg.N * cfg.K
                                                                             + cfg.T * cfg.N) * 2 / 1e9),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
@@ -930,6 +953,9 @@ def main():
     ap.add_argument("--skip-wgrad", action="store_true")
     ap.add_argument("--skip-quant", action="store_true")
     ap.add_argument("--skip-block-scaled", action="store_true")
+    ap.add_argument("--separate-fp", action="store_true",
+                    help="step through moe_grouped_gemm_dprob with separate fingerprint launches for row_src "
+                         "and dprob, instead of moe_grouped_gemm_dprob_fp whose combine takes them")
     ap.add_argument("--no-l2-reserve", action="store_true",
                     help="do not set aside persisting L2 for grad_out (dmoe_reserve_l2_persisting)")
     ap.add_argument("--num-ctas", type=int, default=0, help="persistent CTAs of the GEMM (0 = all resident)")

@@ -78,6 +78,7 @@ def load() -> ctypes.CDLL:
         "moe_token_combine": ([P, P, P, I, I, I, P, P, SZ, P], I),
         "moe_grouped_gemm_fwd": ([P, P, P, I, I, I, I, P, LP, P, SZ, P], I),
         "moe_grouped_gemm_dprob": ([P, P, P, I, I, I, I, P, P, P, I, I, P, P, LP, P, SZ, P], I),
+        "moe_grouped_gemm_dprob_fp": ([P, P, P, I, I, I, I, P, P, P, I, I, P, P, SZ, P, P, LP, P, SZ, P], I),
         "moe_grouped_gemm_dprob_atomic": ([P, P, P, I, I, I, I, P, P, P, I, I, P, LP, P, SZ, P], I),
         "moe_grouped_gemm_dprob_serial": ([P, P, P, I, I, I, I, P, P, P, I, I, P, LP, P, SZ, P], I),
         "moe_grouped_gemm_wgrad": ([P, P, P, I, I, I, I, P, I, LP, P, SZ, P], I),
@@ -266,6 +267,45 @@ def grouped_gemm_dprob(X_perm, W, expert_offsets, grad_out, row_src, topk: int, 
                                        _launch(num_ctas, flags), _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "moe_grouped_gemm_dprob")
     return out, dprob, slots
+
+
+def grouped_gemm_dprob_fp(X_perm, W, expert_offsets, grad_out, row_src, topk: int, ws, out=None, slots=None,
+                          dprob=None, chunk_bytes: int = 1 << 20, row_src_hash=None, dprob_hash=None,
+                          num_ctas: int = 0, stream=None, flags: int = 0):
+    """Deterministic path plus the positional chunk fingerprints of row_src and
+    dprob (those of fingerprint(row_src) and fingerprint(dprob) with the same
+    chunk_bytes).  Returns (expert_out, dprob, slots, row_src_hash, dprob_hash);
+    the hashes are int64 tensors holding uint64 bit patterns."""
+    R, E, K, N = _gemm_shapes(X_perm, W, expert_offsets)
+    T = R // topk
+    dev = X_perm.device
+    S = N // SLOT_COLS
+    nch = fingerprint_num_chunks(R * 4, chunk_bytes)
+    if out is None:
+        out = torch.empty(R, N, dtype=torch.bfloat16, device=dev)
+    if slots is None:
+        slots = torch.empty(S, R, dtype=torch.float32, device=dev)
+    if dprob is None:
+        dprob = torch.empty(T, topk, dtype=torch.float32, device=dev)
+    if row_src_hash is None:
+        row_src_hash = torch.empty(max(nch, 1), dtype=torch.int64, device=dev)
+    if dprob_hash is None:
+        dprob_hash = torch.empty(max(nch, 1), dtype=torch.int64, device=dev)
+    _need(out, torch.bfloat16, "expert_out", (R, N))
+    _need(grad_out, torch.bfloat16, "grad_out", (T, N))
+    _need(row_src, torch.int32, "row_src", (R,))
+    _need(slots, torch.float32, "slots", (S, R))
+    _need(dprob, torch.float32, "dprob", (T, topk))
+    for h, name in ((row_src_hash, "row_src_hash"), (dprob_hash, "dprob_hash")):
+        _need(h, torch.int64, name)
+        if h.numel() < nch:
+            raise ValueError(f"{name} needs {nch} entries")
+    st = load().moe_grouped_gemm_dprob_fp(_ptr(X_perm), _ptr(W), _ptr(expert_offsets), R, E, K, N, _ptr(out),
+                                          _ptr(grad_out), _ptr(row_src), T, topk, _ptr(slots), _ptr(dprob),
+                                          chunk_bytes, _ptr(row_src_hash), _ptr(dprob_hash),
+                                          _launch(num_ctas, flags), _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "moe_grouped_gemm_dprob_fp")
+    return out, dprob, slots, row_src_hash[:nch], dprob_hash[:nch]
 
 
 def grouped_gemm_dprob_atomic(X_perm, W, expert_offsets, grad_out, row_src, topk: int, ws, out=None, dprob=None,

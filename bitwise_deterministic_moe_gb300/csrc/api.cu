@@ -99,6 +99,13 @@ int* status_ptr(void* ws) { return static_cast<int*>(ws); }
 int* sched_ptr(void* ws) { return reinterpret_cast<int*>(static_cast<char*>(ws) + 64); }
 // the routing block scan's finished-block counter at byte 128
 int* route_counter_ptr(void* ws) { return reinterpret_cast<int*>(static_cast<char*>(ws) + 128); }
+// the fingerprinting combine's finished-block counter at byte 132 and its
+// 2 * kFpMaxChunks uint64 accumulators at byte 160 (both left at zero)
+int* fp_done_ptr(void* ws) { return reinterpret_cast<int*>(static_cast<char*>(ws) + 132); }
+unsigned long long* fp_acc_ptr(void* ws) {
+  return reinterpret_cast<unsigned long long*>(static_cast<char*>(ws) + 160);
+}
+static_assert(160 + 2 * kFpMaxChunks * 8 <= DMOE_WS_STATUS_BYTES, "status region layout");
 
 dmoe_status check_gemm_shape(const void* X, const void* W, const int32_t* off, int R, int E, int K, int N,
                              const void* out, void* ws, size_t ws_bytes) {
@@ -245,6 +252,36 @@ dmoe_status moe_grouped_gemm_dprob(const void* X_perm, const void* W, const int3
   cudaError_t e = launch_grouped_gemm(GemmMode::kSlots, a, s);
   if (e != cudaSuccess) return DMOE_ERR_CUDA;
   return cuda_status(launch_dprob_combine(slots, row_src, R, N / DMOE_SLOT_COLS, dprob, s));
+}
+
+dmoe_status moe_grouped_gemm_dprob_fp(const void* X_perm, const void* W, const int32_t* expert_offsets, int R,
+                                      int E, int K, int N, void* expert_out, const void* grad_out,
+                                      const int32_t* row_src, int T, int topk, float* slots, float* dprob,
+                                      size_t chunk_bytes, uint64_t* row_src_hash, uint64_t* dprob_hash,
+                                      const dmoe_launch* launch, void* ws, size_t ws_bytes, dmoe_stream_t stream) {
+  dmoe_status st = check_gemm_shape(X_perm, W, expert_offsets, R, E, K, N, expert_out, ws, ws_bytes);
+  if (st != DMOE_OK) return st;
+  st = check_dprob_args(grad_out, row_src, R, T, topk);
+  if (st != DMOE_OK) return st;
+  if (!slots || !dprob) return DMOE_ERR_INVALID_ARG;
+  if (chunk_bytes == 0 || chunk_bytes % 512 != 0) return DMOE_ERR_INVALID_ARG;
+  if (R > 0 && (!row_src_hash || !dprob_hash)) return DMOE_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  GemmArgs a{};
+  a.X = X_perm; a.W = W; a.offsets = expert_offsets;
+  a.R = R; a.E = E; a.K = K; a.N = N;
+  a.out = expert_out;
+  a.grad_out = grad_out; a.row_src = row_src; a.topk = topk;
+  a.slots = slots;
+  a.status = status_ptr(ws);
+  a.sched = sched_ptr(ws);
+  a.num_ctas = launch ? launch->num_ctas : 0;
+  a.flags = launch ? launch->flags : 0;
+  if (a.num_ctas < 0) return DMOE_ERR_INVALID_ARG;
+  cudaError_t e = launch_grouped_gemm(GemmMode::kSlots, a, s);
+  if (e != cudaSuccess) return DMOE_ERR_CUDA;
+  return cuda_status(launch_dprob_combine_fp(slots, row_src, R, N / DMOE_SLOT_COLS, dprob, chunk_bytes,
+                                             fp_acc_ptr(ws), fp_done_ptr(ws), row_src_hash, dprob_hash, s));
 }
 
 dmoe_status moe_grouped_gemm_dprob_atomic(const void* X_perm, const void* W, const int32_t* expert_offsets, int R,

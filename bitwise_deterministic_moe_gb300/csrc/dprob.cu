@@ -99,18 +99,152 @@ dprob_combine_kernel(const float* __restrict__ slots, const int32_t* __restrict_
   if (unsigned(dst) < unsigned(R)) dprob[dst] = acc;   // a corrupt index is skipped, never written through
 }
 
+// Positional chunk fingerprints of row_src and dprob taken by the combine
+// itself (the mode-0 hash of dmoe_fingerprint: per chunk the sum mod 2^64 of
+// fmix32(word_i ^ i*0x9E3779B9) over its 32-bit words, finalized as
+// sm64(sum ^ (c << 32) ^ chunk_length)).  The combine reads every row_src word
+// and writes every dprob word once, so it forms the terms from values it
+// already holds.  Sums are integers mod 2^64, so the order in which warps and
+// blocks add them does not matter: warp sums go into the block's shared
+// accumulators, block sums into the workspace's, and the last block to finish
+// finalizes the hashes and zeroes the accumulators for the next call.
+struct FpFuse {
+  unsigned long long* acc;   // [2 * kFpMaxChunks] in the workspace: row_src chunks, then dprob chunks
+  int* done;                 // finished-block counter in the workspace
+  unsigned long long* src_hash;
+  unsigned long long* dprob_hash;
+  int chunk_words;           // chunk_bytes / 4, a multiple of 128
+  int nch;                   // chunks of each buffer (R*4 bytes), <= kFpMaxChunks
+};
+
+__device__ __forceinline__ uint32_t fp_fmix32(uint32_t h) {
+  h ^= h >> 16;
+  h *= 0x85EBCA6Bu;
+  h ^= h >> 13;
+  h *= 0xC2B2AE35u;
+  h ^= h >> 16;
+  return h;
+}
+
+__device__ __forceinline__ uint64_t fp_sm64(uint64_t z) {
+  z ^= z >> 30;
+  z *= 0xBF58476D1CE4E5B9ull;
+  z ^= z >> 27;
+  z *= 0x94D049BB133111EBull;
+  z ^= z >> 31;
+  return z;
+}
+
+__device__ __forceinline__ uint64_t fp_term(uint32_t w, uint32_t i) { return fp_fmix32(w ^ (i * 0x9E3779B9u)); }
+
+__device__ __forceinline__ uint64_t warp_sum_u64(uint64_t v) {
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
+  return v;
+}
+
+// One thread's terms (row_src words 4i..4i+3, all in one chunk because a
+// chunk is a multiple of 128 words; dprob words dst.x..w, each in its own
+// chunk) summed per chunk over the warp and the block, then into the
+// workspace; then the thread's dprob stores (a corrupt index skipped, never
+// written through); the last block finalizes.  Every thread of the block
+// calls it (active = 0 for threads past R: no terms, no stores).
+template <bool FP>
+__device__ __forceinline__ void combine_fp_block(const FpFuse& f, int active, int i, int4 dst, float4 v, int R,
+                                                 float* __restrict__ dprob) {
+  __shared__ unsigned long long bacc[2 * kFpMaxChunks];
+  __shared__ int last;
+  const int t = threadIdx.x;
+  const int lane = t & 31;
+  if (t < 2 * kFpMaxChunks) bacc[t] = 0;
+  __syncthreads();
+  uint64_t hs[kFpMaxChunks], hd[kFpMaxChunks];
+#pragma unroll
+  for (int c = 0; c < kFpMaxChunks; ++c) hs[c] = hd[c] = 0;
+  if (active) {
+    const int d[4] = {dst.x, dst.y, dst.z, dst.w};
+    const float x[4] = {v.x, v.y, v.z, v.w};
+    const int cs = (4 * i) / f.chunk_words;
+    uint64_t s4 = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      s4 += fp_term(uint32_t(d[k]), uint32_t(4 * i + k));
+      if (unsigned(d[k]) < unsigned(R)) {
+        const int cd = d[k] / f.chunk_words;
+        const uint64_t term = fp_term(__float_as_uint(x[k]), uint32_t(d[k]));
+#pragma unroll
+        for (int c = 0; c < kFpMaxChunks; ++c)
+          if (c == cd) hd[c] += term;
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < kFpMaxChunks; ++c)
+      if (c == cs) hs[c] += s4;
+  }
+#pragma unroll
+  for (int c = 0; c < kFpMaxChunks; ++c) {
+    if (c >= f.nch) break;
+    if (__any_sync(0xffffffffu, hs[c] != 0)) {
+      const uint64_t w = warp_sum_u64(hs[c]);
+      if (lane == 0) atomicAdd(&bacc[c], (unsigned long long)w);
+    }
+    if (__any_sync(0xffffffffu, hd[c] != 0)) {
+      const uint64_t w = warp_sum_u64(hd[c]);
+      if (lane == 0) atomicAdd(&bacc[kFpMaxChunks + c], (unsigned long long)w);
+    }
+  }
+  __syncthreads();
+  if (t < 2 * kFpMaxChunks) {
+    const unsigned long long b = bacc[t];
+    if (b != 0) atomicAdd(f.acc + t, b);
+    __threadfence();
+  }
+  __syncthreads();
+  if (t == 0) last = atomicAdd(f.done, 1) == int(gridDim.x) - 1;
+  // the dprob stores go out after the block's sums are published, so that the
+  // fence above does not wait for them
+  if (active) {
+    if (unsigned(dst.x) < unsigned(R)) dprob[dst.x] = v.x;
+    if (unsigned(dst.y) < unsigned(R)) dprob[dst.y] = v.y;
+    if (unsigned(dst.z) < unsigned(R)) dprob[dst.z] = v.z;
+    if (unsigned(dst.w) < unsigned(R)) dprob[dst.w] = v.w;
+  }
+  __syncthreads();
+  if (!last) return;
+  // the last block: every other block's sums are in the workspace
+  __threadfence();
+  if (t < 2 * kFpMaxChunks) {
+    const int c = t % kFpMaxChunks;
+    const unsigned long long sum = atomicExch(f.acc + t, 0ull);   // read, and leave zero for the next call
+    if (c < f.nch) {
+      const long long words = (long long)R - (long long)c * f.chunk_words;
+      const uint64_t len = uint64_t(words < f.chunk_words ? words : f.chunk_words) * 4;
+      const uint64_t h = fp_sm64(uint64_t(sum) ^ (uint64_t(c) << 32) ^ len);
+      if (t < kFpMaxChunks) f.src_hash[c] = h;
+      else f.dprob_hash[c] = h;
+    }
+  }
+  if (t == 0) atomicExch(f.done, 0);
+}
+
 // The vectorised form (R % 4 == 0, slots and row_src 16-byte aligned): a
 // thread owns four consecutive rows and reads each slot's four values with
 // one 16-byte load, all of its S loads in flight at once, so the pass moves
 // the slot buffer in few, wide requests.  Each row is still summed on its own
-// in ascending s from slot 0, so the bits equal the general form's.
-template <int S_STATIC>
+// in ascending s from slot 0, so the bits equal the general form's.  FP: also
+// the fingerprints above (every thread then stays to the block's reduction).
+template <int S_STATIC, bool FP>
 __global__ void __launch_bounds__(256)
 dprob_combine_v4_kernel(const float* __restrict__ slots, const int32_t* __restrict__ row_src, int R, int S,
-                        float* __restrict__ dprob) {
+                        float* __restrict__ dprob, FpFuse f) {
   pdl_begin();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;   // group of rows 4i .. 4i+3
-  if (4ll * i >= R) return;
+  const bool active = 4ll * i < R;
+  if (!FP && !active) return;
+  if (FP && !active) {
+    combine_fp_block<FP>(f, 0, 0, make_int4(-1, -1, -1, -1), make_float4(0.f, 0.f, 0.f, 0.f), R, dprob);
+    return;
+  }
   const int nS = S_STATIC > 0 ? S_STATIC : S;
   const float4* p = reinterpret_cast<const float4*>(slots) + i;
   const size_t stride = size_t(R) / 4;                   // one slot, in float4
@@ -136,6 +270,10 @@ dprob_combine_v4_kernel(const float* __restrict__ slots, const int32_t* __restri
     }
   }
   const int4 dst = __ldg(reinterpret_cast<const int4*>(row_src) + i);
+  if (FP) {
+    combine_fp_block<FP>(f, 1, i, dst, acc, R, dprob);   // also stores dprob
+    return;
+  }
   // a corrupt index is skipped, never written through
   if (unsigned(dst.x) < unsigned(R)) dprob[dst.x] = acc.x;
   if (unsigned(dst.y) < unsigned(R)) dprob[dst.y] = acc.y;
@@ -163,11 +301,12 @@ cudaError_t launch_dprob_combine(const float* slots, const int32_t* row_src, int
   const bool v4 = R % 4 == 0 && ((reinterpret_cast<uintptr_t>(slots) | reinterpret_cast<uintptr_t>(row_src)) & 15) == 0;
   if (v4) {
     const unsigned grid = unsigned((R / 4 + 255) / 256);
+    const FpFuse f{};
     switch (S) {
-      case 1: return launch_chained(dprob_combine_v4_kernel<1>, dim3(grid), dim3(256), 0, stream, slots, row_src, R, S, dprob);
-      case 2: return launch_chained(dprob_combine_v4_kernel<2>, dim3(grid), dim3(256), 0, stream, slots, row_src, R, S, dprob);
-      case 16: return launch_chained(dprob_combine_v4_kernel<16>, dim3(grid), dim3(256), 0, stream, slots, row_src, R, S, dprob);
-      default: return launch_chained(dprob_combine_v4_kernel<0>, dim3(grid), dim3(256), 0, stream, slots, row_src, R, S, dprob);
+      case 1: return launch_chained(dprob_combine_v4_kernel<1, false>, dim3(grid), dim3(256), 0, stream, slots, row_src, R, S, dprob, f);
+      case 2: return launch_chained(dprob_combine_v4_kernel<2, false>, dim3(grid), dim3(256), 0, stream, slots, row_src, R, S, dprob, f);
+      case 16: return launch_chained(dprob_combine_v4_kernel<16, false>, dim3(grid), dim3(256), 0, stream, slots, row_src, R, S, dprob, f);
+      default: return launch_chained(dprob_combine_v4_kernel<0, false>, dim3(grid), dim3(256), 0, stream, slots, row_src, R, S, dprob, f);
     }
   }
   const unsigned grid = unsigned((R + 255) / 256);
@@ -176,6 +315,36 @@ cudaError_t launch_dprob_combine(const float* slots, const int32_t* row_src, int
     case 2: return launch_chained(dprob_combine_kernel<2>, dim3(grid), dim3(256), 0, stream, slots, row_src, R, S, dprob);
     case 16: return launch_chained(dprob_combine_kernel<16>, dim3(grid), dim3(256), 0, stream, slots, row_src, R, S, dprob);
     default: return launch_chained(dprob_combine_kernel<0>, dim3(grid), dim3(256), 0, stream, slots, row_src, R, S, dprob);
+  }
+}
+
+cudaError_t launch_dprob_combine_fp(const float* slots, const int32_t* row_src, int R, int S, float* dprob,
+                                    size_t chunk_bytes, unsigned long long* fp_acc, int* fp_done,
+                                    uint64_t* src_hash, uint64_t* dprob_hash, cudaStream_t stream) {
+  if (R == 0) return cudaSuccess;
+  const size_t nbytes = size_t(R) * 4;
+  const size_t nch = (nbytes + chunk_bytes - 1) / chunk_bytes;
+  const bool v4 = R % 4 == 0 && ((reinterpret_cast<uintptr_t>(slots) | reinterpret_cast<uintptr_t>(row_src)) & 15) == 0;
+  if (!v4 || nch > size_t(kFpMaxChunks) || chunk_bytes % 512 != 0 || chunk_bytes / 4 > 0x7FFFFFFFull) {
+    // the combine, then a separate fingerprint pass over each buffer
+    cudaError_t e = launch_dprob_combine(slots, row_src, R, S, dprob, stream);
+    if (e == cudaSuccess) e = launch_fingerprint(row_src, nbytes, 4, 0, chunk_bytes, 0, src_hash, stream);
+    if (e == cudaSuccess) e = launch_fingerprint(dprob, nbytes, 4, 0, chunk_bytes, 0, dprob_hash, stream);
+    return e;
+  }
+  FpFuse f;
+  f.acc = fp_acc;
+  f.done = fp_done;
+  f.src_hash = reinterpret_cast<unsigned long long*>(src_hash);
+  f.dprob_hash = reinterpret_cast<unsigned long long*>(dprob_hash);
+  f.chunk_words = int(chunk_bytes / 4);
+  f.nch = int(nch);
+  const unsigned grid = unsigned((R / 4 + 255) / 256);
+  switch (S) {
+    case 1: return launch_chained(dprob_combine_v4_kernel<1, true>, dim3(grid), dim3(256), 0, stream, slots, row_src, R, S, dprob, f);
+    case 2: return launch_chained(dprob_combine_v4_kernel<2, true>, dim3(grid), dim3(256), 0, stream, slots, row_src, R, S, dprob, f);
+    case 16: return launch_chained(dprob_combine_v4_kernel<16, true>, dim3(grid), dim3(256), 0, stream, slots, row_src, R, S, dprob, f);
+    default: return launch_chained(dprob_combine_v4_kernel<0, true>, dim3(grid), dim3(256), 0, stream, slots, row_src, R, S, dprob, f);
   }
 }
 

@@ -96,6 +96,14 @@ cudaError_t launch_dprob_epilogue(const void* grad_out, const void* expert_out, 
                                   int* status, cudaStream_t stream);
 cudaError_t launch_dprob_combine(const float* slots, const int32_t* row_src, int R, int S, float* dprob,
                                  cudaStream_t stream);
+// The combine plus the positional chunk fingerprints of row_src and dprob,
+// taken inside the combine when each buffer has at most kFpMaxChunks chunks
+// (accumulators and a finished-block counter in the workspace, left zero);
+// otherwise the combine and two fingerprint launches.
+constexpr int kFpMaxChunks = 6;
+cudaError_t launch_dprob_combine_fp(const float* slots, const int32_t* row_src, int R, int S, float* dprob,
+                                    size_t chunk_bytes, unsigned long long* fp_acc, int* fp_done,
+                                    uint64_t* src_hash, uint64_t* dprob_hash, cudaStream_t stream);
 
 // fingerprint
 cudaError_t launch_fingerprint(const void* data, size_t nbytes, int elem_size, int xor_kind, size_t chunk_bytes,

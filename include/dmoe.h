@@ -213,6 +213,36 @@ dmoe_status moe_grouped_gemm_dprob(const void* X_perm, const void* W, const int3
                                    dmoe_stream_t stream);
 
 /*
+ * The deterministic path with the fingerprints of its order-sensitive data
+ * ("NVIDIA fait passer ...", section "Méthodologie de débogage du
+ * non-déterminisme": the routing map and the outputs are fingerprinted on the
+ * GPU, chunk by chunk): moe_grouped_gemm_dprob, and in the same call the
+ * mode-0 (positional, raw bits) chunk hashes of row_src and of dprob exactly
+ * as dmoe_fingerprint computes them with the same chunk_bytes.  The combine
+ * reads every row_src word and writes every dprob word, so it forms the hash
+ * terms itself, with no further pass over memory, when each buffer (R*4
+ * bytes) has at most 6 chunks and the combine takes its vectorised form
+ * (R % 4 == 0, slots and row_src 16-byte aligned); otherwise the call runs a
+ * fingerprint pass over each buffer after the combine.  The header hashes
+ * (dtype, shape) are the caller's, as for dmoe_fingerprint.  If row_src is
+ * not a permutation of [0, R) the dprob hash covers the values the combine
+ * wrote, which may differ from the buffer's.
+ *   chunk_bytes   > 0, a multiple of 512
+ *   row_src_hash  uint64 [dmoe_fingerprint_num_chunks(R*4, chunk_bytes)] out
+ *   dprob_hash    uint64 [dmoe_fingerprint_num_chunks(R*4, chunk_bytes)] out
+ * The status region of ws holds the sums between the combine's blocks and is
+ * left at zero, so calls sharing ws must be ordered on one stream (as for
+ * every call).  Other arguments and errors as for moe_grouped_gemm_dprob.
+ */
+dmoe_status moe_grouped_gemm_dprob_fp(const void* X_perm, const void* W, const int32_t* expert_offsets,
+                                      int R, int E, int K, int N, void* expert_out,
+                                      const void* grad_out, const int32_t* row_src, int T, int topk,
+                                      float* slots, float* dprob,
+                                      size_t chunk_bytes, uint64_t* row_src_hash, uint64_t* dprob_hash,
+                                      const dmoe_launch* launch, void* ws, size_t ws_bytes,
+                                      dmoe_stream_t stream);
+
+/*
  * L2 residency of grad_out for the dprob epilogue.  Every grad_out row is
  * gathered by topk different tiles at different times while the weights and
  * expert_out stream through L2; the epilogue loads it with an L2 evict-last
