@@ -22,6 +22,7 @@ slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import atexit
 import json
 import math
 import os
@@ -117,8 +118,13 @@ class ClockSampler:
                  "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            atexit.register(self._kill)   # no sampler outlives the process, even after an error
         except Exception:
             self.proc = None
+
+    def _kill(self):
+        if self.proc is not None and self.proc.poll() is None:
+            self.proc.kill()
 
     def _read(self):
         for line in self.proc.stdout:
@@ -491,6 +497,11 @@ def run_ours(args):
             ev[1].record(stream)
         api.fingerprint(dprob, out=fp_dp)
 
+    # the clock sampler starts (and takes its first samples) before the
+    # warm-up steps, so that no idle pause separates them from the timed steps
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
@@ -501,17 +512,16 @@ def run_ours(args):
     flops, abytes = algorithmic(cfg, off_np)
 
     # ---------------- timed region: K steps, inputs resident in HBM (> L2)
-    # The GEMM call is bracketed by events on every EV_EVERY-th step only: an
-    # event between two programmatically chained launches exposes the next
-    # launch's latency (~6 us a step with events on every step).
+    # The GEMM call is bracketed by events on the last step of every group of
+    # ev_every steps only: an event between two programmatically chained
+    # launches exposes the next launch's latency (~6 us a step with events on
+    # every step), and the first timed step follows the host's checks above
+    # after a short pause.
     ev_every = max(1, min(4, args.steps // 3))
     gemm_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               if i % ev_every == 0 else None for i in range(args.steps)]
+               if i % ev_every == ev_every - 1 else None for i in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.3)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
