@@ -125,12 +125,15 @@ def test_relabel_and_token_permutation_bitwise():
     assert torch.equal(out2.view(torch.int16)[rows_new], out0.view(torch.int16)[rows_base])
 
 
+@pytest.mark.parametrize("fused", [False, True], ids=["separate_fp", "fused_fp"])
 @pytest.mark.parametrize("name", ["small", "latent"])
-def test_cuda_graph_replay_bitwise(name):
+def test_cuda_graph_replay_bitwise(name, fused):
     """The whole step (routing, fingerprint, GEMM + slots + combine,
     fingerprint) captured once in a CUDA graph and replayed gives the eager
     bits: every launch is graph-capturable (programmatic launches included)
-    and the workspace counters reset themselves between replays."""
+    and the workspace counters reset themselves between replays.  fused: the
+    fingerprints taken by the combine (moe_grouped_gemm_dprob_fp), whose
+    cross-block sums live in the workspace; they equal the separate ones."""
     cfg = synth.CONFIGS[name]
     prob = Problem(cfg)
     ids = torch.from_numpy(prob.inp.topk_ids).cuda()
@@ -143,16 +146,29 @@ def test_cuda_graph_replay_bitwise(name):
     fp_src = torch.empty(nch, dtype=torch.int64, device="cuda")
     fp_dp = torch.empty(nch, dtype=torch.int64, device="cuda")
 
-    def step():
+    def step_separate():
         api.permute_indices(ids, cfg.E, prob.ws, off, src)
         api.fingerprint(src, out=fp_src)
         api.grouped_gemm_dprob(prob.X, prob.W, off, prob.G, src, cfg.topk, prob.ws, out=out, slots=slots,
                                dprob=dprob)
         api.fingerprint(dprob, out=fp_dp)
 
-    step()
+    def step_fused():
+        api.permute_indices(ids, cfg.E, prob.ws, off, src)
+        api.grouped_gemm_dprob_fp(prob.X, prob.W, off, prob.G, src, cfg.topk, prob.ws, out=out, slots=slots,
+                                  dprob=dprob, row_src_hash=fp_src, dprob_hash=fp_dp)
+
+    step_separate()
     torch.cuda.synchronize()
     ref = [t.clone() for t in (off, src, out, slots, dprob, fp_src, fp_dp)]
+    step = step_fused if fused else step_separate
+    if fused:
+        for t in (fp_src, fp_dp):
+            t.zero_()
+        step()
+        torch.cuda.synchronize()
+        for a, b in zip(ref, (off, src, out, slots, dprob, fp_src, fp_dp)):
+            assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
     for t in (off, src, out, slots, dprob, fp_src, fp_dp):
         t.zero_()
     s = torch.cuda.Stream()
