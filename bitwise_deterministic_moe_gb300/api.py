@@ -47,6 +47,7 @@ class _Launch(ctypes.Structure):
 LAUNCH_TEST_STALL = 1
 LAUNCH_SINGLE_CTA = 2   # force the one-SM-per-tile kernel
 LAUNCH_CTA_PAIRS = 4    # force the 2-SM (CTA pair) kernel
+LAUNCH_NARROW_TILES = 8  # block-scaled MXFP8: one-slot (128 x 128) tiles only
 
 
 _lib = None
@@ -444,7 +445,7 @@ def quantize_nvfp4(x: torch.Tensor, ws: torch.Tensor, packed=None, scales=None, 
 
 # ------------------------------------------------------------------ block-scaled grouped GEMM
 def _block_scaled(kind, Xq, Xs, Xg, Wq, Ws, Wg, expert_offsets, K, grad_out, row_src, topk, ws, out, slots, dprob,
-                  num_ctas, stream):
+                  num_ctas, stream, flags=0):
     R = Xq.shape[0]
     E = expert_offsets.numel() - 1
     N = Wq.shape[1]
@@ -478,24 +479,24 @@ def _block_scaled(kind, Xq, Xs, Xg, Wq, Ws, Wg, expert_offsets, K, grad_out, row
     if kind == 0:
         st = lib.moe_grouped_gemm_dprob_mxfp8(_ptr(Xq), _ptr(Xs), _ptr(Wq), _ptr(Ws), _ptr(expert_offsets), R, E, K, N,
                                               _ptr(out), _ptr(grad_out), _ptr(row_src), T, topk, _ptr(slots),
-                                              _ptr(dprob), _launch(num_ctas), _ptr(ws), ws.numel(), _stream(stream))
+                                              _ptr(dprob), _launch(num_ctas, flags), _ptr(ws), ws.numel(), _stream(stream))
         _check(st, "moe_grouped_gemm_dprob_mxfp8")
     else:
         st = lib.moe_grouped_gemm_dprob_nvfp4(_ptr(Xq), _ptr(Xs), _ptr(Xg), _ptr(Wq), _ptr(Ws), _ptr(Wg),
                                               _ptr(expert_offsets), R, E, K, N, _ptr(out), _ptr(grad_out),
-                                              _ptr(row_src), T, topk, _ptr(slots), _ptr(dprob), _launch(num_ctas),
+                                              _ptr(row_src), T, topk, _ptr(slots), _ptr(dprob), _launch(num_ctas, flags),
                                               _ptr(ws), ws.numel(), _stream(stream))
         _check(st, "moe_grouped_gemm_dprob_nvfp4")
     return out, dprob, slots
 
 
 def grouped_gemm_dprob_mxfp8(X_q, X_scales, W_q, W_scales, expert_offsets, grad_out, row_src, topk: int, ws,
-                             out=None, slots=None, dprob=None, num_ctas: int = 0, stream=None):
+                             out=None, slots=None, dprob=None, num_ctas: int = 0, stream=None, flags: int = 0):
     """MXFP8 operands (E4M3 codes [R, K], [E, N, K]; E8M0 scales [R, K/32], [E*N, K/32]):
     returns (expert_out bf16 [R, N], dprob, slots); grad_out None = forward only (dprob, slots None)."""
     K = X_q.shape[1]
     return _block_scaled(0, X_q, X_scales, None, W_q, W_scales, None, expert_offsets, K, grad_out, row_src, topk, ws,
-                         out, slots, dprob, num_ctas, stream)
+                         out, slots, dprob, num_ctas, stream, flags)
 
 
 def grouped_gemm_dprob_nvfp4(X_packed, X_scales, X_s_enc, W_packed, W_scales, W_s_enc, expert_offsets, grad_out,

@@ -475,6 +475,7 @@ static dmoe_status block_scaled_call(int kind, const uint8_t* Xq, const uint8_t*
   a.status = status_ptr(ws);
   a.sched = sched_ptr(ws);
   a.num_ctas = launch ? launch->num_ctas : 0;
+  a.narrow = (launch && (launch->flags & DMOE_LAUNCH_NARROW_TILES)) ? 1 : 0;
   if (launch_grouped_gemm_block_scaled(a, s) != cudaSuccess) return DMOE_ERR_CUDA;
   if (!grad_out) return DMOE_OK;
   return cuda_status(launch_dprob_combine(slots, row_src, R, N / DMOE_SLOT_COLS, dprob, s));

@@ -92,18 +92,26 @@ static_assert(BN == SLOT, "one tile is one slot");
 //          8 columns each; every MMA takes a whole word): 32 columns.  An
 //          MMA's scale address must sit on a multiple of 4 columns, so the
 //          four MMAs of a stage read A at columns 4 kk and B at 16 + 4 kk.
-template <int KIND>
+//   TW = 2 (MXFP8 only): a tile is two adjacent slots (128 x 256) -- the
+//          stage's A box feeds two N = 128 MMAs, one per slot, with B boxes
+//          (and their scale boxes and blocks) for both halves: 4 + 4 + 4
+//          scale columns a stage (16 with the 4-column alignment), three
+//          stages, and one 256-column accumulator pair.
+template <int KIND, int TW>
 struct Layout {
-  static constexpr int OFF_B = A_BYTES;
-  static constexpr int OFF_SFA_BOX = A_BYTES + B_BYTES;
-  static constexpr int OFF_SFB_BOX = OFF_SFA_BOX + SFBOX_BYTES;
-  static constexpr int OFF_SFA_BLK = OFF_SFB_BOX + SFBOX_BYTES;
+  static_assert(TW == 1 || (TW == 2 && KIND == 0), "two-slot tiles are MXFP8 only");
+  static constexpr int OFF_B = A_BYTES;                  // B box of slot h at OFF_B + h * B_BYTES
+  static constexpr int OFF_SFA_BOX = A_BYTES + TW * B_BYTES;
+  static constexpr int OFF_SFB_BOX = OFF_SFA_BOX + SFBOX_BYTES;   // slot h at + h * SFBOX_BYTES
+  static constexpr int OFF_SFA_BLK = OFF_SFB_BOX + TW * SFBOX_BYTES;
   static constexpr int SRC_BYTES = KIND == 0 ? SFBLK_BYTES : SF256_BYTES;
-  static constexpr int OFF_SFB_BLK = OFF_SFA_BLK + (KIND == 0 ? 1 : 2) * SRC_BYTES;
-  static constexpr int STAGE_BYTES = ((OFF_SFB_BLK + (KIND == 0 ? 1 : 2) * SRC_BYTES) + 1023) / 1024 * 1024;
-  static constexpr int SF_COLS_STAGE = KIND == 0 ? 8 : 32;
-  static constexpr int STAGES = KIND == 0 ? 5 : 4;
-  static_assert(TMEM_SF0 + STAGES * SF_COLS_STAGE <= TMEM_COLS, "tensor memory");
+  static constexpr int OFF_SFB_BLK = OFF_SFA_BLK + (KIND == 0 ? 1 : 2) * SRC_BYTES;   // slot h at + h * SRC_BYTES
+  static constexpr int STAGE_BYTES = ((OFF_SFB_BLK + TW * (KIND == 0 ? 1 : 2) * SRC_BYTES) + 1023) / 1024 * 1024;
+  static constexpr int SF_COLS_STAGE = KIND == 0 ? (TW == 1 ? 8 : 16) : 32;
+  static constexpr int STAGES = KIND == 0 ? (TW == 1 ? 5 : 3) : 4;
+  static constexpr int ACC = TW == 1 ? ACC_BUFS : 1;     // accumulators (of TW slots each)
+  static constexpr int SF0 = ACC * TW * BN;              // first scale column
+  static_assert(SF0 + STAGES * SF_COLS_STAGE <= TMEM_COLS, "tensor memory");
   static constexpr size_t SMEM = 1024 + size_t(STAGES) * STAGE_BYTES + size_t(EPI_WARPS) * STG_BYTES + 1024;
   static_assert(SMEM <= 232448, "dynamic shared memory above the 227 KB a CTA may use");
 };
@@ -226,14 +234,14 @@ __device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdes
   asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
-template <int KIND, int MODE>
+template <int KIND, int MODE, int TW>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                        const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
                        const __grid_constant__ CUtensorMap tmap_o, const KParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  using L = Layout<KIND>;
+  using L = Layout<KIND, TW>;
   Ctrl& c = *reinterpret_cast<Ctrl*>(base + size_t(L::STAGES) * L::STAGE_BYTES + size_t(EPI_WARPS) * STG_BYTES);
   const uint32_t stage0 = smem_u32(base);
 
@@ -249,9 +257,10 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
       mbar_init(smem_u32(&c.sfrdy[s]), 1);
       mbar_init(smem_u32(&c.empty[s]), 1);
     }
-    for (int b = 0; b < ACC_BUFS; ++b) {
+    for (int b = 0; b < L::ACC; ++b) {
       mbar_init(smem_u32(&c.acc_full[b]), 1);
-      mbar_init(smem_u32(&c.acc_empty[b]), 4);   // the four warps of the group that took the tile
+      // the four warps of the group that took the tile (TW = 2: both groups, one slot each)
+      mbar_init(smem_u32(&c.acc_empty[b]), 4 * TW);
     }
     mbar_init(smem_u32(&c.mma_done), 1);
     for (int i = 0; i < TQ; ++i) {
@@ -297,14 +306,17 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
           const uint32_t sa = stage0 + stage * L::STAGE_BYTES;
           const uint32_t full = smem_u32(&c.full[stage]);
           const uint32_t sfin = smem_u32(&c.sfin[stage]);
-          mbar_arrive_expect_tx(full, A_BYTES + B_BYTES);
+          mbar_arrive_expect_tx(full, A_BYTES + TW * B_BYTES);
           tma_load_2d(sa, &tmap_a, full, kb * ROWB, tl.row0);
-          tma_load_2d(sa + L::OFF_B, &tmap_b, full, kb * ROWB, brow);
+#pragma unroll
+          for (int h = 0; h < TW; ++h) tma_load_2d(sa + L::OFF_B + h * B_BYTES, &tmap_b, full, kb * ROWB, brow + h * BN);
           // 16 bytes of scales per row: four stages' words (MXFP8) or this stage's four (NVFP4)
           const int sx = KIND == kMxf8 ? 16 * (kb >> 2) : 16 * kb;
-          mbar_arrive_expect_tx(sfin, 2 * SFBOX_BYTES);
+          mbar_arrive_expect_tx(sfin, (1 + TW) * SFBOX_BYTES);
           tma_load_2d(sa + L::OFF_SFA_BOX, &tmap_sfa, sfin, sx, tl.row0);
-          tma_load_2d(sa + L::OFF_SFB_BOX, &tmap_sfb, sfin, sx, brow);
+#pragma unroll
+          for (int h = 0; h < TW; ++h)
+            tma_load_2d(sa + L::OFF_SFB_BOX + h * SFBOX_BYTES, &tmap_sfb, sfin, sx, brow + h * BN);
           ++issued_total;
           if (++stage == L::STAGES) { stage = 0; ph ^= 1u; }
         }
@@ -334,18 +346,20 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
         if (cur < 0) break;
         if (!mbar_wait(smem_u32(&c.acc_empty[acc]), aph ^ 1u, &c.abort, p.status, p.wait_ns)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
+        const uint32_t d_tmem = tmem_base + uint32_t(acc * TW * BN);   // slot h at + h * BN
         bool ok = true;
         for (int kb = 0; kb < p.KB; ++kb) {
           if (!mbar_wait(smem_u32(&c.full[stage]), ph, &c.abort, p.status, p.wait_ns)) { ok = false; break; }
           if (!mbar_wait(smem_u32(&c.sfrdy[stage]), ph, &c.abort, p.status, p.wait_ns)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = stage0 + stage * L::STAGE_BYTES;
-          const uint32_t sfc = tmem_base + uint32_t(TMEM_SF0 + stage * L::SF_COLS_STAGE);
+          const uint32_t sfc = tmem_base + uint32_t(L::SF0 + stage * L::SF_COLS_STAGE);
           // scale sources -> tensor memory (ordered before the MMAs this thread issues next)
           if (KIND == kMxf8) {
             tmem_cp_32x128b_x4(sfc, smem_desc_sfblk(sa + L::OFF_SFA_BLK));
-            tmem_cp_32x128b_x4(sfc + 4u, smem_desc_sfblk(sa + L::OFF_SFB_BLK));
+#pragma unroll
+            for (int h = 0; h < TW; ++h)
+              tmem_cp_32x128b_x4(sfc + 4u + 4u * uint32_t(h), smem_desc_sfblk(sa + L::OFF_SFB_BLK + h * SFBLK_BYTES));
           } else {
             tmem_cp_128x256b(sfc, smem_desc_sf256(sa + L::OFF_SFA_BLK));
             tmem_cp_128x256b(sfc + 8u, smem_desc_sf256(sa + L::OFF_SFA_BLK + SF256_BYTES));
@@ -353,7 +367,6 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
             tmem_cp_128x256b(sfc + 24u, smem_desc_sf256(sa + L::OFF_SFB_BLK + SF256_BYTES));
           }
           const uint64_t adesc = smem_desc_k128(sa);
-          const uint64_t bdesc = smem_desc_k128(sa + L::OFF_B);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             // 32 bytes of each row per MMA: 32 E4M3 or 64 E2M1 values.  MXFP8:
@@ -362,16 +375,21 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
             // of the stage's scale columns
             const uint32_t sfid = KIND == kMxf8 ? uint32_t(kk) : 0u;
             const uint32_t sfa = KIND == kMxf8 ? sfc : sfc + 4u * uint32_t(kk);
-            const uint32_t sfb = KIND == kMxf8 ? sfc + 4u : sfc + 16u + 4u * uint32_t(kk);
-            bs_mma<KIND>(d_tmem, adesc + uint64_t(kk * 2), bdesc + uint64_t(kk * 2), bs_idesc<KIND>(sfid), sfa, sfb,
-                         (kb | kk) != 0 ? 1u : 0u);
+#pragma unroll
+            for (int h = 0; h < TW; ++h) {
+              // slot h: its own B box, scale block and accumulator; the A box is shared
+              const uint32_t sfb = KIND == kMxf8 ? sfc + 4u + 4u * uint32_t(h) : sfc + 16u + 4u * uint32_t(kk);
+              const uint64_t bdesc = smem_desc_k128(sa + L::OFF_B + h * B_BYTES);
+              bs_mma<KIND>(d_tmem + uint32_t(h * BN), adesc + uint64_t(kk * 2), bdesc + uint64_t(kk * 2),
+                           bs_idesc<KIND>(sfid), sfa, sfb, (kb | kk) != 0 ? 1u : 0u);
+            }
           }
           tc_commit(smem_u32(&c.empty[stage]));
           if (++stage == L::STAGES) { stage = 0; ph ^= 1u; }
         }
         if (!ok) break;
         tc_commit(smem_u32(&c.acc_full[acc]));
-        if (++acc == ACC_BUFS) { acc = 0; aph ^= 1u; }
+        if (++acc == L::ACC) { acc = 0; aph ^= 1u; }
       }
       tc_commit(smem_u32(&c.mma_done));
       mbar_wait_drain(smem_u32(&c.mma_done), 0, p.wait_ns / 4);
@@ -401,9 +419,10 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
         if (!warp_wait(smem_u32(&c.sfin[stage]), ph, &c.abort, p.status, lane, p.wait_ns)) { ok = false; break; }
         const uint32_t sa = stage0 + stage * L::STAGE_BYTES;
 #pragma unroll
-        for (int op = 0; op < 2; ++op) {
-          const uint32_t box = sa + (op == 0 ? L::OFF_SFA_BOX : L::OFF_SFB_BOX);
-          const uint32_t blk = sa + (op == 0 ? L::OFF_SFA_BLK : L::OFF_SFB_BLK);
+        for (int op = 0; op < 1 + TW; ++op) {
+          // op 0: A; op 1 + h: B of slot h
+          const uint32_t box = sa + (op == 0 ? L::OFF_SFA_BOX : L::OFF_SFB_BOX + (op - 1) * SFBOX_BYTES);
+          const uint32_t blk = sa + (op == 0 ? L::OFF_SFA_BLK : L::OFF_SFB_BLK + (op - 1) * L::SRC_BYTES);
           uint4 r[4];
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc) r[cc] = lds_v4(box + uint32_t((32 * cc + lane) * 16));
@@ -452,7 +471,7 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
       if (cur >= 0 && lane == 0) nxt = int(gridDim.x) + atomicAdd(p.sched, 1);
       QTile q{};
       q.cur = -1;
-      if (cur >= 0) q = decode_tile_warp<BM, BN>(cur, tb, E, p.NT, units_heavy, units, lane);
+      if (cur >= 0) q = decode_tile_warp<BM, TW * BN>(cur, tb, E, p.NT, units_heavy, units, lane);
       if (!warp_wait(smem_u32(&c.tq_empty[qs]), uint32_t((qi / TQ) & 1) ^ 1u, &c.abort, p.status, lane, p.wait_ns))
         break;
       if (lane == 0) {
@@ -464,11 +483,14 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
     }
   } else {
     // -------------------------------------------------- epilogue (2 groups of 4 warps)
-    // Group g takes the CTA's tiles g, g+2, g+4, ...; tile i sits in
-    // accumulator i % 3.  Every epilogue warp reads every queue entry (to see
-    // the end marker).  Warp w reads TMEM lanes 32*(w%4)..+31: 32 rows x the
-    // tile's 128 columns (one slot).  Same staging, stores and fixed in-slot
-    // tree as the bf16 single-CTA kernel.
+    // TW = 1: group g takes the CTA's tiles g, g+2, g+4, ...; tile i sits in
+    // accumulator i % 3.  TW = 2: both groups take every tile, group g its
+    // slot g; each warp first drains its 32 rows x 128 columns into registers
+    // as bf16 (the values it stores and dots), then frees the accumulator, so
+    // the next tile's MMAs wait only for that drain.  Every epilogue warp reads
+    // every queue entry (to see the end marker).  Warp w reads TMEM lanes
+    // 32*(w%4)..+31.  Same staging, stores and fixed in-slot tree as the bf16
+    // single-CTA kernel.
     const int q = warp & 3;
     const int grp = (warp - EPI_WARP0) >> 2;
     const int k4 = lane & 3;
@@ -486,11 +508,11 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&c.tq_empty[qs]));
       if (cur < 0) break;
-      if ((qi & 1) != grp) {
-        if (++acc == ACC_BUFS) { acc = 0; aph ^= 1u; }
+      if (TW == 1 && (qi & 1) != grp) {
+        if (++acc == L::ACC) { acc = 0; aph ^= 1u; }
         continue;
       }
-      const int col0 = tl.n0;
+      const int col0 = tl.n0 + (TW == 2 ? grp * BN : 0);
       int rr[4], src[4];
       bool ok[4];
 #pragma unroll
@@ -500,7 +522,6 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
         src[i] = 0;
       }
       const bool full32 = tl.row0 + q * 32 + 32 <= tl.row_end;
-      uint4 g[16];
       if (MODE != int(GemmMode::kFwd)) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -512,6 +533,93 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
             }
           }
         }
+      }
+      if (TW == 2) {
+        if (!warp_wait(smem_u32(&c.acc_full[acc]), aph, &c.abort, p.status, lane, p.wait_ns)) break;
+        tc_fence_after();
+        const uint32_t tcol = tmem_base + uint32_t(acc * TW * BN + grp * BN) + (uint32_t(q * 32) << 16);
+        // drain: row `lane` of the warp's quarter, four chunks of 32 columns, as bf16
+        uint4 yb[4][4];
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tcol + uint32_t(ch * 32), v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            yb[ch][kk].x = pack_bf16x2_rn(__uint_as_float(v[8 * kk + 0]), __uint_as_float(v[8 * kk + 1]));
+            yb[ch][kk].y = pack_bf16x2_rn(__uint_as_float(v[8 * kk + 2]), __uint_as_float(v[8 * kk + 3]));
+            yb[ch][kk].z = pack_bf16x2_rn(__uint_as_float(v[8 * kk + 4]), __uint_as_float(v[8 * kk + 5]));
+            yb[ch][kk].w = pack_bf16x2_rn(__uint_as_float(v[8 * kk + 6]), __uint_as_float(v[8 * kk + 7]));
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&c.acc_empty[acc]));
+        if (++acc == L::ACC) { acc = 0; aph ^= 1u; }
+        // grad_out of the rows the lane dots, one chunk ahead of use
+        const uint16_t* gp[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          gp[i] = p.grad_out + size_t(ok[i] ? src[i] / p.topk : 0) * p.N + (ok[i] ? col0 : 0) + k4 * 8;
+        uint4 gc[4], gn[4];
+        if (MODE != int(GemmMode::kFwd)) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) gc[i] = ok[i] ? ldg_nc_v4_hint(gp[i], pol_keep) : make_uint4(0, 0, 0, 0);
+        }
+        float a[4][8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) a[i][j] = 0.0f;
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          if (MODE != int(GemmMode::kFwd) && ch + 1 < 4) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              gn[i] = ok[i] ? ldg_nc_v4_hint(gp[i] + (ch + 1) * 32, pol_keep) : make_uint4(0, 0, 0, 0);
+          }
+          if (lane == 0) bulk_wait_group_read<0>();   // the previous chunk's store has read the staging
+          __syncwarp();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) sts_v4(stg + uint32_t(lane * 64 + ((kk ^ ((lane >> 1) & 3)) << 4)), yb[ch][kk]);
+          __syncwarp();
+          if (full32) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmap_o, stg, col0 + ch * 32, tl.row0 + q * 32);
+              bulk_commit_group();
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int row = i * 8 + (lane >> 2);
+            const uint4 y = lds_v4(stg + uint32_t(row * 64 + ((k4 ^ ((row >> 1) & 3)) << 4)));
+            if (ok[i]) {
+              if (!full32) stg_v4(p.out + size_t(rr[i]) * p.N + col0 + ch * 32 + k4 * 8, y);
+              if (MODE != int(GemmMode::kFwd)) slot_accumulate8(a[i], gc[i], y);
+            }
+          }
+          __syncwarp();
+          if (MODE != int(GemmMode::kFwd)) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) gc[i] = gn[i];
+          }
+        }
+        if (MODE != int(GemmMode::kFwd)) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float part = slot_tree(a[i]);
+            part = __fadd_rn(part, __shfl_xor_sync(0xffffffffu, part, 1));
+            part = __fadd_rn(part, __shfl_xor_sync(0xffffffffu, part, 2));
+            if (k4 == 0 && ok[i]) p.slots[size_t(col0 / SLOT) * p.R + rr[i]] = part;
+          }
+        }
+        continue;
+      }
+      uint4 g[16];
+      if (MODE != int(GemmMode::kFwd)) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const uint16_t* gp = p.grad_out + size_t(ok[i] ? src[i] / p.topk : 0) * p.N + (ok[i] ? col0 : 0) + k4 * 8;
@@ -521,7 +629,7 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
       }
       if (!warp_wait(smem_u32(&c.acc_full[acc]), aph, &c.abort, p.status, lane, p.wait_ns)) break;
       tc_fence_after();
-      const uint32_t tcol = tmem_base + uint32_t(acc * BN) + (uint32_t(q * 32) << 16);
+      const uint32_t tcol = tmem_base + uint32_t(acc * BN) + (uint32_t(q * 32) << 16);   // TW = 1
       float a[4][8];
 #pragma unroll
       for (int i = 0; i < 4; ++i)
@@ -579,7 +687,7 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&c.acc_empty[acc]));
-      if (++acc == ACC_BUFS) { acc = 0; aph ^= 1u; }
+      if (++acc == L::ACC) { acc = 0; aph ^= 1u; }
     }
     if (lane == 0) bulk_wait_group_all();
   }
@@ -602,13 +710,13 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
   }
 }
 
-template <int KIND, int MODE>
+template <int KIND, int MODE, int TW>
 cudaError_t launch_kind_mode(const CUtensorMap* maps, const KParams& kp, int grid, cudaStream_t stream) {
-  using L = Layout<KIND>;
+  using L = Layout<KIND, TW>;
   const cudaError_t e =
-      ensure_kernel_smem(reinterpret_cast<const void*>(grouped_gemm_bs_kernel<KIND, MODE>), int(L::SMEM));
+      ensure_kernel_smem(reinterpret_cast<const void*>(grouped_gemm_bs_kernel<KIND, MODE, TW>), int(L::SMEM));
   if (e != cudaSuccess) return e;
-  return launch_chained(grouped_gemm_bs_kernel<KIND, MODE>, dim3(grid), dim3(NUM_THREADS), L::SMEM, stream,
+  return launch_chained(grouped_gemm_bs_kernel<KIND, MODE, TW>, dim3(grid), dim3(NUM_THREADS), L::SMEM, stream,
                         maps[0], maps[1], maps[2], maps[3], maps[4], kp);
 }
 
@@ -640,7 +748,9 @@ cudaError_t launch_grouped_gemm_block_scaled(const BlockScaledArgs& a, cudaStrea
   kp.R = a.R;
   kp.K = a.K;
   kp.N = a.N;
-  kp.NT = a.N / BN;
+  // MXFP8 with an even number of slots: two-slot tiles, unless narrow tiles are asked for
+  const int tw = (!nvf4 && (a.N / BN) % 2 == 0 && !a.narrow) ? 2 : 1;
+  kp.NT = a.N / (BN * tw);
   kp.KB = int(kbytes / ROWB);
   kp.out = static_cast<uint16_t*>(a.out);
   kp.grad_out = static_cast<const uint16_t*>(a.grad_out);
@@ -656,11 +766,14 @@ cudaError_t launch_grouped_gemm_block_scaled(const BlockScaledArgs& a, cudaStrea
   const int grid = a.num_ctas > 0 ? a.num_ctas : device_sm_count();
   const bool fwd = a.grad_out == nullptr;
   if (!nvf4) {
-    return fwd ? launch_kind_mode<kMxf8, int(GemmMode::kFwd)>(maps, kp, grid, stream)
-               : launch_kind_mode<kMxf8, int(GemmMode::kSlots)>(maps, kp, grid, stream);
+    if (tw == 2)
+      return fwd ? launch_kind_mode<kMxf8, int(GemmMode::kFwd), 2>(maps, kp, grid, stream)
+                 : launch_kind_mode<kMxf8, int(GemmMode::kSlots), 2>(maps, kp, grid, stream);
+    return fwd ? launch_kind_mode<kMxf8, int(GemmMode::kFwd), 1>(maps, kp, grid, stream)
+               : launch_kind_mode<kMxf8, int(GemmMode::kSlots), 1>(maps, kp, grid, stream);
   }
-  return fwd ? launch_kind_mode<kNvf4, int(GemmMode::kFwd)>(maps, kp, grid, stream)
-             : launch_kind_mode<kNvf4, int(GemmMode::kSlots)>(maps, kp, grid, stream);
+  return fwd ? launch_kind_mode<kNvf4, int(GemmMode::kFwd), 1>(maps, kp, grid, stream)
+             : launch_kind_mode<kNvf4, int(GemmMode::kSlots), 1>(maps, kp, grid, stream);
 }
 
 }  // namespace dmoe

@@ -52,6 +52,7 @@ struct BlockScaledArgs {
   int* status;
   int* sched;
   int num_ctas;
+  int narrow;                 // MXFP8: one-slot tiles even when N allows two-slot ones
 };
 cudaError_t launch_grouped_gemm_block_scaled(const BlockScaledArgs& a, cudaStream_t stream);
 

@@ -73,6 +73,8 @@ typedef enum dmoe_dtype {
  * at the resident count.  flags, OR-ed:
  *   DMOE_LAUNCH_SINGLE_CTA  force the single-CTA kernel
  *   DMOE_LAUNCH_CTA_PAIRS   force the CTA-pair kernel
+ *   DMOE_LAUNCH_NARROW_TILES  block-scaled MXFP8 calls: one-slot (128 x 128)
+ *     tiles even where N allows two-slot (128 x 256) ones; same bits
  *   DMOE_LAUNCH_TEST_STALL  exercise the failure path: the first CTA arms one
  *     pipeline stage but never loads it, so the wait on it runs out (after a
  *     200 ms limit instead of the usual 2 s), the kernel records
@@ -85,6 +87,7 @@ typedef struct dmoe_launch {
 #define DMOE_LAUNCH_TEST_STALL 1
 #define DMOE_LAUNCH_SINGLE_CTA 2
 #define DMOE_LAUNCH_CTA_PAIRS 4
+#define DMOE_LAUNCH_NARROW_TILES 8
 
 /* Supported shapes of the grouped GEMM calls:
  *   1 <= E <= DMOE_MAX_EXPERTS, 8 <= K <= 65536 with K % 8 == 0,
@@ -457,8 +460,11 @@ dmoe_status dmoe_quantize_nvfp4(const void* x, int rows, int cols, uint8_t* pack
  * Accumulation is fp32 on the tensor cores in a fixed k order, so results
  * are bitwise identical for any num_ctas and any stream; device-side errors
  * (offsets, row_src) go to the workspace status word as in
- * moe_grouped_gemm_dprob.  launch->flags is ignored (one kernel: 128 x 128
- * tiles on single CTAs).
+ * moe_grouped_gemm_dprob.  Tiles run on single CTAs: MXFP8 with an even
+ * number of 128-column slots (N % 256 == 0) uses 128 x 256 tiles (the A
+ * operand shared by the two slots' MMAs), otherwise 128 x 128; both give the
+ * same bits, and launch->flags = DMOE_LAUNCH_NARROW_TILES forces 128 x 128.
+ * Other flags are ignored.
  */
 dmoe_status moe_grouped_gemm_dprob_mxfp8(const uint8_t* X_q, const uint8_t* X_scales, const uint8_t* W_q,
                                          const uint8_t* W_scales, const int32_t* expert_offsets, int R, int E, int K,

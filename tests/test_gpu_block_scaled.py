@@ -51,14 +51,14 @@ class Encoded:
         kb = cfg.K if kind == "mxfp8" else cfg.K // 2
         self.wq3 = self.wq.view(cfg.E, cfg.N, kb)
 
-    def run(self, prob, grad=True, num_ctas=0, stream=None, out=None, slots=None, dprob=None):
+    def run(self, prob, grad=True, num_ctas=0, stream=None, out=None, slots=None, dprob=None, flags=0):
         cfg = prob.cfg
         G = prob.G if grad else None
         src = prob.src if grad else None
         if self.kind == "mxfp8":
             return api.grouped_gemm_dprob_mxfp8(self.xq, self.xs, self.wq3, self.ws, prob.off, G, src, cfg.topk,
                                                 prob.ws, out=out, slots=slots, dprob=dprob, num_ctas=num_ctas,
-                                                stream=stream)
+                                                stream=stream, flags=flags)
         return api.grouped_gemm_dprob_nvfp4(self.xq, self.xs, self.xg, self.wq3, self.ws, self.wg, prob.off, G, src,
                                             cfg.topk, prob.ws, out=out, slots=slots, dprob=dprob, num_ctas=num_ctas,
                                             stream=stream)
@@ -246,3 +246,28 @@ def test_nvfp4_single_stage_k256():
     rows = np.arange(cfg.R)
     Y, Yb, P, D, src = oracle_rows(prob, "nvfp4", rows, check_codes=enc)
     gpu_util.compare_rows(out, slots, dprob, rows, Y, Yb, P, D, src, prob.inp.G, cfg.topk)
+
+
+@pytest.mark.parametrize("name", ["bs_small", "bs_zipf", "latent"])
+def test_mxfp8_two_slot_tiles_equal_one_slot_tiles(name):
+    """MXFP8 with N % 256 == 0 runs 128 x 256 tiles (the two slots' MMAs
+    share the A operand); forcing 128 x 128 tiles gives the same bits:
+    expert_out, slots and dprob, forward and dprob calls, two grid sizes."""
+    cfg = synth.CONFIGS[name] if name in synth.CONFIGS else next(c for c in SHAPES if c.name == name)
+    assert cfg.N % 256 == 0
+    prob = Problem(cfg)
+    enc = Encoded(prob, "mxfp8")
+    wide = enc.run(prob)
+    wide = tuple(t.clone() for t in wide)
+    narrow = enc.run(prob, flags=api.LAUNCH_NARROW_TILES)
+    for a, b in zip(wide, narrow):
+        assert torch.equal(a.view(torch.int32) if a.dtype == torch.float32 else a.view(torch.int16),
+                           b.view(torch.int32) if b.dtype == torch.float32 else b.view(torch.int16))
+    fw = enc.run(prob, grad=False)[0].clone()
+    fn = enc.run(prob, grad=False, flags=api.LAUNCH_NARROW_TILES)[0]
+    assert torch.equal(fw.view(torch.int16), fn.view(torch.int16))
+    assert torch.equal(fw.view(torch.int16), wide[0].view(torch.int16))
+    o, d, s_ = enc.run(prob, num_ctas=37)
+    assert torch.equal(o.view(torch.int16), wide[0].view(torch.int16))
+    assert torch.equal(d.view(torch.int32), wide[1].view(torch.int32))
+    assert api.read_status(prob.ws) == 0
