@@ -498,4 +498,41 @@ __device__ __forceinline__ void stg_v4(void* p, const uint4& v) {
                : "memory");
 }
 
+// ---------------------------------------------------------------- register transposes
+__device__ __forceinline__ uint4 shfl_xor_u4(const uint4& v, int m) {
+  uint4 r;
+  r.x = __shfl_xor_sync(0xffffffffu, v.x, m);
+  r.y = __shfl_xor_sync(0xffffffffu, v.y, m);
+  r.z = __shfl_xor_sync(0xffffffffu, v.z, m);
+  r.w = __shfl_xor_sync(0xffffffffu, v.w, m);
+  return r;
+}
+
+// 4 x 4 transpose of 16-byte pieces inside each quad of lanes: lane 4a + b
+// enters with pieces 0..3 of its own row and leaves with piece b of rows
+// 4a + 0 .. 4a + 3 (two exchange rounds, across lane bits 0 and 1).
+// Lane-dependent choices are made with masks, element by element, so the
+// pieces are never addressed through an index (they must stay in registers).
+__device__ __forceinline__ uint4 mask_sel(uint32_t m, const uint4& a, const uint4& b) {   // m ? a : b
+  return make_uint4((a.x & m) | (b.x & ~m), (a.y & m) | (b.y & ~m), (a.z & m) | (b.z & ~m), (a.w & m) | (b.w & ~m));
+}
+
+__device__ __forceinline__ void quad_transpose(uint4 (&x)[4], int lane) {
+  const uint32_t odd = (lane & 1) ? 0xffffffffu : 0u;
+#pragma unroll
+  for (int j = 0; j < 4; j += 2) {
+    const uint4 r = shfl_xor_u4(mask_sel(odd, x[j], x[j + 1]), 1);
+    x[j] = mask_sel(odd, r, x[j]);
+    x[j + 1] = mask_sel(odd, x[j + 1], r);
+  }
+  const uint32_t hi = (lane & 2) ? 0xffffffffu : 0u;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const uint4 r = shfl_xor_u4(mask_sel(hi, x[j], x[j + 2]), 2);
+    x[j] = mask_sel(hi, r, x[j]);
+    x[j + 2] = mask_sel(hi, x[j + 2], r);
+  }
+}
+
+
 }  // namespace dmoe

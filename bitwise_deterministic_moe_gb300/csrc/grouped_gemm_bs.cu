@@ -68,7 +68,7 @@ constexpr int SFBOX_BYTES = 128 * 16;         // TMA box of scale bytes: 128 row
 constexpr int SFBLK_BYTES = 32 * 16;          // one .32x128b tcgen05.cp source: 32 rows x 16 bytes
 constexpr int SF256_BYTES = 128 * 32;         // one .128x256b tcgen05.cp source: 128 rows x 32 bytes
 constexpr int ACC_BUFS = 3;
-constexpr int TMEM_SF0 = ACC_BUFS * BN;       // scale columns after the accumulators
+
 constexpr int TMEM_COLS = 512;
 constexpr int EPI_WARP0 = 2;
 constexpr int EPI_GROUPS = 2;
@@ -95,8 +95,9 @@ static_assert(BN == SLOT, "one tile is one slot");
 //   TW = 2 (MXFP8 only): a tile is two adjacent slots (128 x 256) -- the
 //          stage's A box feeds two N = 128 MMAs, one per slot, with B boxes
 //          (and their scale boxes and blocks) for both halves: 4 + 4 + 4
-//          scale columns a stage (16 with the 4-column alignment), three
-//          stages, and one 256-column accumulator pair.
+//          scale columns a stage (16 with the 4-column alignment), one
+//          256-column accumulator pair, and four stages: the epilogue stores
+//          from registers, so it needs no staging buffers.
 template <int KIND, int TW>
 struct Layout {
   static_assert(TW == 1 || (TW == 2 && KIND == 0), "two-slot tiles are MXFP8 only");
@@ -108,11 +109,12 @@ struct Layout {
   static constexpr int OFF_SFB_BLK = OFF_SFA_BLK + (KIND == 0 ? 1 : 2) * SRC_BYTES;   // slot h at + h * SRC_BYTES
   static constexpr int STAGE_BYTES = ((OFF_SFB_BLK + TW * (KIND == 0 ? 1 : 2) * SRC_BYTES) + 1023) / 1024 * 1024;
   static constexpr int SF_COLS_STAGE = KIND == 0 ? (TW == 1 ? 8 : 16) : 32;
-  static constexpr int STAGES = KIND == 0 ? (TW == 1 ? 5 : 3) : 4;
+  static constexpr int STAGES = KIND == 0 ? (TW == 1 ? 5 : 4) : 4;
   static constexpr int ACC = TW == 1 ? ACC_BUFS : 1;     // accumulators (of TW slots each)
   static constexpr int SF0 = ACC * TW * BN;              // first scale column
   static_assert(SF0 + STAGES * SF_COLS_STAGE <= TMEM_COLS, "tensor memory");
-  static constexpr size_t SMEM = 1024 + size_t(STAGES) * STAGE_BYTES + size_t(EPI_WARPS) * STG_BYTES + 1024;
+  static constexpr int STAGING = TW == 1 ? EPI_WARPS * STG_BYTES : 0;   // per-warp TMA store staging
+  static constexpr size_t SMEM = 1024 + size_t(STAGES) * STAGE_BYTES + size_t(STAGING) + 1024;
   static_assert(SMEM <= 232448, "dynamic shared memory above the 227 KB a CTA may use");
 };
 constexpr int MAX_STAGES = 5;
@@ -242,7 +244,7 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   using L = Layout<KIND, TW>;
-  Ctrl& c = *reinterpret_cast<Ctrl*>(base + size_t(L::STAGES) * L::STAGE_BYTES + size_t(EPI_WARPS) * STG_BYTES);
+  Ctrl& c = *reinterpret_cast<Ctrl*>(base + size_t(L::STAGES) * L::STAGE_BYTES + size_t(L::STAGING));
   const uint32_t stage0 = smem_u32(base);
 
   const int tid = threadIdx.x;
@@ -495,7 +497,7 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
     const int grp = (warp - EPI_WARP0) >> 2;
     const int k4 = lane & 3;
     const uint64_t pol_keep = policy_evict_last();
-    const uint32_t stg = stage0 + uint32_t(L::STAGES * L::STAGE_BYTES + (warp - EPI_WARP0) * STG_BYTES);
+    const uint32_t stg = stage0 + uint32_t(L::STAGES * L::STAGE_BYTES + (warp - EPI_WARP0) * STG_BYTES);   // TW = 1
     float alpha = 1.0f;
     if (KIND == kNvf4) alpha = __frcp_rn(__fmul_rn(__ldg(p.s_enc_x), __ldg(p.s_enc_w)));
     int acc = 0;
@@ -515,9 +517,13 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
       const int col0 = tl.n0 + (TW == 2 ? grp * BN : 0);
       int rr[4], src[4];
       bool ok[4];
+      // the rows whose 16-byte piece k4 this lane stores and dots: TW = 1,
+      // rows 8i + lane/4 (the staging buffer's read-back layout); TW = 2,
+      // rows 4 (lane/4) + i (after a quad transpose of the lane's own row, as
+      // in the CTA-pair kernel)
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        rr[i] = tl.row0 + q * 32 + i * 8 + (lane >> 2);
+        rr[i] = tl.row0 + q * 32 + (TW == 2 ? (lane & ~3) + i : i * 8 + (lane >> 2));
         ok[i] = rr[i] < tl.row_end;
         src[i] = 0;
       }
@@ -538,7 +544,9 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
         if (!warp_wait(smem_u32(&c.acc_full[acc]), aph, &c.abort, p.status, lane, p.wait_ns)) break;
         tc_fence_after();
         const uint32_t tcol = tmem_base + uint32_t(acc * TW * BN + grp * BN) + (uint32_t(q * 32) << 16);
-        // drain: row `lane` of the warp's quarter, four chunks of 32 columns, as bf16
+        // drain: row `lane` of the warp's quarter, four chunks of 32 columns, as
+        // bf16, each chunk quad-transposed at once (yb[ch][i] = piece k4 of row
+        // 4 (lane/4) + i)
         uint4 yb[4][4];
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
@@ -552,6 +560,7 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
             yb[ch][kk].z = pack_bf16x2_rn(__uint_as_float(v[8 * kk + 4]), __uint_as_float(v[8 * kk + 5]));
             yb[ch][kk].w = pack_bf16x2_rn(__uint_as_float(v[8 * kk + 6]), __uint_as_float(v[8 * kk + 7]));
           }
+          quad_transpose(yb[ch], lane);
         }
         tc_fence_before();
         __syncwarp();
@@ -579,29 +588,13 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
             for (int i = 0; i < 4; ++i)
               gn[i] = ok[i] ? ldg_nc_v4_hint(gp[i] + (ch + 1) * 32, pol_keep) : make_uint4(0, 0, 0, 0);
           }
-          if (lane == 0) bulk_wait_group_read<0>();   // the previous chunk's store has read the staging
-          __syncwarp();
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) sts_v4(stg + uint32_t(lane * 64 + ((kk ^ ((lane >> 1) & 3)) << 4)), yb[ch][kk]);
-          __syncwarp();
-          if (full32) {
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              tma_store_2d(&tmap_o, stg, col0 + ch * 32, tl.row0 + q * 32);
-              bulk_commit_group();
-            }
-          }
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const int row = i * 8 + (lane >> 2);
-            const uint4 y = lds_v4(stg + uint32_t(row * 64 + ((k4 ^ ((row >> 1) & 3)) << 4)));
             if (ok[i]) {
-              if (!full32) stg_v4(p.out + size_t(rr[i]) * p.N + col0 + ch * 32 + k4 * 8, y);
-              if (MODE != int(GemmMode::kFwd)) slot_accumulate8(a[i], gc[i], y);
+              stg_v4(p.out + size_t(rr[i]) * p.N + col0 + ch * 32 + k4 * 8, yb[ch][i]);
+              if (MODE != int(GemmMode::kFwd)) slot_accumulate8(a[i], gc[i], yb[ch][i]);
             }
           }
-          __syncwarp();
           if (MODE != int(GemmMode::kFwd)) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) gc[i] = gn[i];
