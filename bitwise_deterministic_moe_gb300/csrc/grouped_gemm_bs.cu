@@ -541,6 +541,17 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
         }
       }
       if (TW == 2) {
+        // grad_out of the rows the lane dots: chunk 0 before the accumulator
+        // is ready, then one chunk ahead of use
+        const uint16_t* gp[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          gp[i] = p.grad_out + size_t(ok[i] ? src[i] / p.topk : 0) * p.N + (ok[i] ? col0 : 0) + k4 * 8;
+        uint4 gc[4], gn[4];
+        if (MODE != int(GemmMode::kFwd)) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) gc[i] = ok[i] ? ldg_nc_v4_hint(gp[i], pol_keep) : make_uint4(0, 0, 0, 0);
+        }
         if (!warp_wait(smem_u32(&c.acc_full[acc]), aph, &c.abort, p.status, lane, p.wait_ns)) break;
         tc_fence_after();
         const uint32_t tcol = tmem_base + uint32_t(acc * TW * BN + grp * BN) + (uint32_t(q * 32) << 16);
@@ -566,16 +577,6 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&c.acc_empty[acc]));
         if (++acc == L::ACC) { acc = 0; aph ^= 1u; }
-        // grad_out of the rows the lane dots, one chunk ahead of use
-        const uint16_t* gp[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          gp[i] = p.grad_out + size_t(ok[i] ? src[i] / p.topk : 0) * p.N + (ok[i] ? col0 : 0) + k4 * 8;
-        uint4 gc[4], gn[4];
-        if (MODE != int(GemmMode::kFwd)) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) gc[i] = ok[i] ? ldg_nc_v4_hint(gp[i], pol_keep) : make_uint4(0, 0, 0, 0);
-        }
         float a[4][8];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
