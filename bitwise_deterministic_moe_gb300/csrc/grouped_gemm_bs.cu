@@ -310,15 +310,14 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
           const uint32_t sfin = smem_u32(&c.sfin[stage]);
           mbar_arrive_expect_tx(full, A_BYTES + TW * B_BYTES);
           tma_load_2d(sa, &tmap_a, full, kb * ROWB, tl.row0);
-#pragma unroll
-          for (int h = 0; h < TW; ++h) tma_load_2d(sa + L::OFF_B + h * B_BYTES, &tmap_b, full, kb * ROWB, brow + h * BN);
+          // B (and below its scales): one box of TW * 128 rows -- the tensor
+          // maps' box height -- whose slot-h half lands at + h * B_BYTES
+          tma_load_2d(sa + L::OFF_B, &tmap_b, full, kb * ROWB, brow);
           // 16 bytes of scales per row: four stages' words (MXFP8) or this stage's four (NVFP4)
           const int sx = KIND == kMxf8 ? 16 * (kb >> 2) : 16 * kb;
           mbar_arrive_expect_tx(sfin, (1 + TW) * SFBOX_BYTES);
           tma_load_2d(sa + L::OFF_SFA_BOX, &tmap_sfa, sfin, sx, tl.row0);
-#pragma unroll
-          for (int h = 0; h < TW; ++h)
-            tma_load_2d(sa + L::OFF_SFB_BOX + h * SFBOX_BYTES, &tmap_sfb, sfin, sx, brow + h * BN);
+          tma_load_2d(sa + L::OFF_SFB_BOX, &tmap_sfb, sfin, sx, brow);
           ++issued_total;
           if (++stage == L::STAGES) { stage = 0; ph ^= 1u; }
         }
@@ -726,13 +725,15 @@ cudaError_t launch_grouped_gemm_block_scaled(const BlockScaledArgs& a, cudaStrea
   if (!make_tmap_2d(&maps[0], a.Xq, u8, uint64_t(a.R), kbytes, kbytes, ROWB, BM, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
     return cudaErrorInvalidValue;
-  if (!make_tmap_2d(&maps[1], a.Wq, u8, uint64_t(a.E) * a.N, kbytes, kbytes, ROWB, BN, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
+  // MXFP8 with an even number of slots: two-slot tiles, unless narrow tiles are asked for
+  const int tw = (!nvf4 && (a.N / BN) % 2 == 0 && !a.narrow) ? 2 : 1;
+  if (!make_tmap_2d(&maps[1], a.Wq, u8, uint64_t(a.E) * a.N, kbytes, kbytes, ROWB, BN * tw,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
     return cudaErrorInvalidValue;
   if (!make_tmap_2d(&maps[2], a.Xs, u8, uint64_t(a.R), sbytes, sbytes, 16, BM, CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_NONE))
     return cudaErrorInvalidValue;
-  if (!make_tmap_2d(&maps[3], a.Ws, u8, uint64_t(a.E) * a.N, sbytes, sbytes, 16, BN, CU_TENSOR_MAP_SWIZZLE_NONE,
+  if (!make_tmap_2d(&maps[3], a.Ws, u8, uint64_t(a.E) * a.N, sbytes, sbytes, 16, BN * tw, CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_NONE))
     return cudaErrorInvalidValue;
   if (!make_tmap_bf16_store32(&maps[4], a.out, uint64_t(a.R), uint64_t(a.N))) return cudaErrorInvalidValue;
@@ -742,8 +743,6 @@ cudaError_t launch_grouped_gemm_block_scaled(const BlockScaledArgs& a, cudaStrea
   kp.R = a.R;
   kp.K = a.K;
   kp.N = a.N;
-  // MXFP8 with an even number of slots: two-slot tiles, unless narrow tiles are asked for
-  const int tw = (!nvf4 && (a.N / BN) % 2 == 0 && !a.narrow) ? 2 : 1;
   kp.NT = a.N / (BN * tw);
   kp.KB = int(kbytes / ROWB);
   kp.out = static_cast<uint16_t*>(a.out);
