@@ -810,6 +810,10 @@ def run_ours(args):
                                  "why": "timed region %.3f s: %s" % (ms_max * 1e-3,
                                         "under 1 s, burst figure" if peak_kind == "burst"
                                         else "1 s or longer, sustained figure")},
+                 # the combined bound max(flops / tensor peak, bytes / HBM peak) and the
+                 # fraction of it the call reaches
+                 "combined_bound": {"ms": max(t_tc, t_hbm) * 1e3, "tensor_ms": t_tc * 1e3, "hbm_ms": t_hbm * 1e3,
+                                    "frac": max(t_tc, t_hbm) / gemm_s},
                  "tensor_frac_of_burst": achieved_tf / burst,
                  "tensor_frac_of_sustained": achieved_tf / sustained,
                  "hbm_frac": achieved_gbs / pk["hbm_gbs"],
