@@ -200,6 +200,14 @@ def cpu_baseline(cfg, inp, target_s=12.0, full_configs=()):
     res = {"value": flops / t / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
            "sample": f"{n} of {cfg.R} permuted rows of the {cfg.name} workload (GEMM+bf16+slots+dprob, fp64), "
                      f"{t:.1f} s"}
+    # the whole oracle on the larger configs, extrapolated from this sample:
+    # its cost per row is one K x N row product plus the row's slots, so it
+    # scales with R * K * N (labelled as an extrapolation, not a run)
+    per_row_kn = t / (n * cfg.K * cfg.N)
+    res["extrapolated_full_oracle"] = {
+        name: {"s": per_row_kn * c.R * c.K * c.N, "rows": c.R,
+               "basis": f"the {cfg.name} sample's time per row scaled by R*K*N (not run)"}
+        for name, c in ((nm, synth.CONFIGS[nm]) for nm in ("imbal", "stress"))}
     if full_configs:
         # the whole oracle (routing, every row's GEMM, bf16 output, slots, dprob)
         # on the configs small enough to finish in seconds
