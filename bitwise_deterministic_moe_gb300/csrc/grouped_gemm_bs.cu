@@ -542,10 +542,12 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
       if (TW == 2) {
         // grad_out of the rows the lane dots: chunk 0 before the accumulator
         // is ready, then one chunk ahead of use
-        const uint16_t* gp[4];
+        const uint16_t* gp[4] = {nullptr, nullptr, nullptr, nullptr};   // forward only: no grad_out
+        if (MODE != int(GemmMode::kFwd)) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          gp[i] = p.grad_out + size_t(ok[i] ? src[i] / p.topk : 0) * p.N + (ok[i] ? col0 : 0) + k4 * 8;
+          for (int i = 0; i < 4; ++i)
+            gp[i] = p.grad_out + size_t(ok[i] ? src[i] / p.topk : 0) * p.N + (ok[i] ? col0 : 0) + k4 * 8;
+        }
         uint4 gc[4], gn[4];
         if (MODE != int(GemmMode::kFwd)) {
 #pragma unroll
