@@ -177,11 +177,13 @@ def test_block_scaled_forward_only_and_repeatability(kind):
 
 
 @pytest.mark.parametrize("kind", KINDS)
-def test_block_scaled_latent_sampled_rows(kind):
-    """The LatentMoE-shaped workload at full size (T=8192, E=512, top-22,
-    K=1024, N=2048), on rows of twelve experts (the hottest, the lightest
-    non-empty and ten others) that the oracle computes one by one."""
-    cfg = synth.CONFIGS["latent"]
+@pytest.mark.parametrize("name", ["latent", "stress"])
+def test_block_scaled_latent_sampled_rows(kind, name):
+    """Full-size workloads -- LatentMoE-shaped (T=8192, E=512, top-22,
+    K=1024, N=2048) and the stress size (T=32768, K=2048) -- on rows of
+    twelve experts (the hottest, the lightest non-empty and ten others) that
+    the oracle computes one by one."""
+    cfg = synth.CONFIGS[name]
     prob = Problem(cfg)
     enc = Encoded(prob, kind)
     out, dprob, slots = enc.run(prob)
