@@ -166,7 +166,7 @@ def test_wgrad_zero_rows():
     assert bool((dW == 0).all())
 
 
-@pytest.mark.parametrize("name", ["latent", "imbal"])
+@pytest.mark.parametrize("name", ["latent", "imbal", "stress"])
 def test_wgrad_full_size_sampled(name):
     cfg = synth.CONFIGS[name]
     prob = WProblem(cfg)
