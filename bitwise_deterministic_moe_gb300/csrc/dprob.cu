@@ -137,6 +137,8 @@ __device__ __forceinline__ uint64_t fp_sm64(uint64_t z) {
 
 __device__ __forceinline__ uint64_t fp_term(uint32_t w, uint32_t i) { return fp_fmix32(w ^ (i * 0x9E3779B9u)); }
 
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 __device__ __forceinline__ uint64_t warp_sum_u64(uint64_t v) {
 #pragma unroll
   for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
@@ -197,10 +199,16 @@ __device__ __forceinline__ void combine_fp_block(const FpFuse& f, int active, in
   if (t < 2 * kFpMaxChunks) {
     const unsigned long long b = bacc[t];
     if (b != 0) atomicAdd(f.acc + t, b);
-    __threadfence();
   }
   __syncthreads();
-  if (t == 0) last = atomicAdd(f.done, 1) == int(gridDim.x) - 1;
+  if (t == 0) {
+    // release: the fence is cumulative over the block's adds above (ordered
+    // before it by the barrier), so they are visible before the count; on the
+    // last block, acquire every other block's adds before the reads below
+    fence_acq_rel_gpu();
+    last = atomicAdd(f.done, 1) == int(gridDim.x) - 1;
+    if (last) fence_acq_rel_gpu();
+  }
   // the dprob stores go out after the block's sums are published, so that the
   // fence above does not wait for them
   if (active) {
@@ -211,8 +219,8 @@ __device__ __forceinline__ void combine_fp_block(const FpFuse& f, int active, in
   }
   __syncthreads();
   if (!last) return;
-  // the last block: every other block's sums are in the workspace
-  __threadfence();
+  // the last block: every other block's sums are in the workspace (thread 0's
+  // acquire, ordered before these reads by the barrier)
   if (t < 2 * kFpMaxChunks) {
     const int c = t % kFpMaxChunks;
     const unsigned long long sum = atomicExch(f.acc + t, 0ull);   // read, and leave zero for the next call
