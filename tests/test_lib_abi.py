@@ -27,6 +27,19 @@ def declared_functions():
     return sorted(set(names))
 
 
+def test_binding_constants_match_the_header():
+    """The binding's launch flags and limits are the header's #defines."""
+    from bitwise_deterministic_moe_gb300 import api
+    defines = dict(re.findall(r"^#define (DMOE_\w+) (\d+)", open(HEADER).read(), flags=re.M))
+    pairs = {"DMOE_LAUNCH_TEST_STALL": api.LAUNCH_TEST_STALL, "DMOE_LAUNCH_SINGLE_CTA": api.LAUNCH_SINGLE_CTA,
+             "DMOE_LAUNCH_CTA_PAIRS": api.LAUNCH_CTA_PAIRS, "DMOE_LAUNCH_NARROW_TILES": api.LAUNCH_NARROW_TILES,
+             "DMOE_SLOT_COLS": api.SLOT_COLS, "DMOE_MAX_EXPERTS": api.MAX_EXPERTS}
+    for name, value in pairs.items():
+        assert int(defines[name]) == value, name
+    flags = [v for k, v in pairs.items() if k.startswith("DMOE_LAUNCH_")]
+    assert all(f & (f - 1) == 0 for f in flags) and len(set(flags)) == len(flags)   # distinct single bits
+
+
 def test_header_declares_the_boundary():
     names = declared_functions()
     for want in ["moe_grouped_gemm_fwd", "moe_grouped_gemm_dprob", "moe_grouped_gemm_dprob_atomic",
