@@ -812,7 +812,7 @@ def run_ours(args):
                                 "moe_grouped_gemm_dprob_fp (the same call, its combine also fingerprinting row_src and dprob)",
                  "single_call_runs": "moe_grouped_gemm_dprob (call_l2_flushed, call_l2_hot)",
                  "algorithmic_bytes": abytes, "algorithmic_flops": flops,
-                 "peak_source": f"{pk_kind} ({PEAKS_FILE if pk_kind == 'measured' else 'profiling recipe'})",
+                 "peak_source": f"{pk_kind} ({os.path.basename(PEAKS_FILE) if pk_kind == 'measured' else 'profiling recipe'})",
                  "tensor_frac": achieved_tf / tc_peak, "tensor_tflops": achieved_tf,
                  "tensor_peak": {"tflops": tc_peak, "kind": peak_kind,
                                  "why": "timed region %.3f s: %s" % (ms_max * 1e-3,
