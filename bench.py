@@ -789,13 +789,27 @@ def run_ours(args):
         e_ms = max_over_ranks(a.elapsed_time(b), world)
         h2d = sum(t.numel() * t.element_size() for t in (h_ids, h_X, h_G))
         d2h = sum(t.numel() * t.element_size() for t in (h_dprob, h_fp, h_fps))
+        # the host link's own rate on this machine: the same per-step input copies
+        # alone, back to back on the copy stream (median of five)
+        link_ms = []
+        for _ in range(5):
+            la, lb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            la.record(copy_stream)
+            with torch.cuda.stream(copy_stream):
+                for dst, hsrc in zip(sets[1], (h_ids, h_X, h_G)):
+                    dst.copy_(hsrc, non_blocking=True)
+            lb.record(copy_stream)
+            torch.cuda.synchronize(dev)
+            link_ms.append(la.elapsed_time(lb))
+        link_ms = float(np.median(link_ms))
         e2e = {"value": whole_job_tflops(flops, args.e2e_steps, world, e_ms), "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": e_ms / args.e2e_steps,
                "copied": "topk_ids, X_perm, grad_out in (pinned host -> device, every step, the next step's "
                          "copy overlapping the current step's compute); dprob and both fingerprints out; "
                          "expert weights resident",
-               "bitwise_equal_to_resident": bool(torch.equal(h_dprob, ref_dprob) and torch.equal(h_fp, ref_fp))}
+               "bitwise_equal_to_resident": bool(torch.equal(h_dprob, ref_dprob) and torch.equal(h_fp, ref_fp)),
+               "h2d_copy_alone_ms": link_ms, "h2d_copy_alone_gbs": h2d / (link_ms * 1e-3) / 1e9}
 
     # digests of the step's outputs (chunk fingerprints folded with the header):
     # identical inputs give identical digests on every run
