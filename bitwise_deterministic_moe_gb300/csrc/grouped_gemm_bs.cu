@@ -92,12 +92,15 @@ static_assert(BN == SLOT, "one tile is one slot");
 //          8 columns each; every MMA takes a whole word): 32 columns.  An
 //          MMA's scale address must sit on a multiple of 4 columns, so the
 //          four MMAs of a stage read A at columns 4 kk and B at 16 + 4 kk.
-//   TW = 2 (MXFP8 only): a tile is two adjacent slots (128 x 256) -- the
-//          stage's A box feeds two N = 128 MMAs, one per slot, with B boxes
-//          (and their scale boxes and blocks) for both halves: 4 + 4 + 4
-//          scale columns a stage (16 with the 4-column alignment), one
-//          256-column accumulator pair, and four stages: the epilogue stores
-//          from registers, so it needs no staging buffers.
+//   TW = 2 (MXFP8 only): a tile is two adjacent slots (128 x 256) -- one
+//          256-row B box and one N = 256 MMA per 32-byte step over both
+//          slots (fewer, wider MMAs keep the tensor pipe busier than two
+//          N = 128 MMAs sharing the A box; each output element's sum is the
+//          same), the B scales of the two halves in adjacent 4-column blocks
+//          (row r at column r / 32 across them): 4 + 8 scale columns a stage
+//          (16 with the 4-column alignment), one 256-column accumulator
+//          pair, and four stages: the epilogue stores from registers, so it
+//          needs no staging buffers.
 template <int KIND, int TW>
 struct Layout {
   static_assert(TW == 1 || (TW == 2 && KIND == 0), "two-slot tiles are MXFP8 only");
@@ -198,11 +201,12 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {   // i is a
 // Instruction descriptor of the block-scaled kinds: B scale id (bits 4-5),
 // A and B formats (7-9, 10-12), both K-major, N >> 3 (17-22), scale format
 // (23: 1 = E8M0, 0 = E4M3), M >> 4 (24-28), A scale id (29-30).
-template <int KIND>
+template <int KIND, int N>
 __device__ __forceinline__ uint32_t bs_idesc(uint32_t sf_id) {
+  static_assert(N % 16 == 0 && N >= 16 && N <= 256, "UMMA N");
   constexpr uint32_t fmt = KIND == kMxf8 ? 0u : 1u;          // E4M3 in mxf8f6f4 / E2M1 in mxf4nvf4
   constexpr uint32_t sfmt = KIND == kMxf8 ? 1u : 0u;
-  return (sf_id << 4) | (fmt << 7) | (fmt << 10) | (uint32_t(BN >> 3) << 17) | (sfmt << 23) |
+  return (sf_id << 4) | (fmt << 7) | (fmt << 10) | (uint32_t(N >> 3) << 17) | (sfmt << 23) |
          (uint32_t(BM >> 4) << 24) | (sf_id << 29);
 }
 
@@ -376,14 +380,13 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
             // of the stage's scale columns
             const uint32_t sfid = KIND == kMxf8 ? uint32_t(kk) : 0u;
             const uint32_t sfa = KIND == kMxf8 ? sfc : sfc + 4u * uint32_t(kk);
-#pragma unroll
-            for (int h = 0; h < TW; ++h) {
-              // slot h: its own B box, scale block and accumulator; the A box is shared
-              const uint32_t sfb = KIND == kMxf8 ? sfc + 4u + 4u * uint32_t(h) : sfc + 16u + 4u * uint32_t(kk);
-              const uint64_t bdesc = smem_desc_k128(sa + L::OFF_B + h * B_BYTES);
-              bs_mma<KIND>(d_tmem + uint32_t(h * BN), adesc + uint64_t(kk * 2), bdesc + uint64_t(kk * 2),
-                           bs_idesc<KIND>(sfid), sfa, sfb, (kb | kk) != 0 ? 1u : 0u);
-            }
+            // one MMA over the tile's TW slots: B rows 0 .. TW*128-1 (one box),
+            // their scales in the columns from sfc + 4 (MXFP8) on, the
+            // accumulators of the slots side by side
+            const uint32_t sfb = KIND == kMxf8 ? sfc + 4u : sfc + 16u + 4u * uint32_t(kk);
+            const uint64_t bdesc = smem_desc_k128(sa + L::OFF_B);
+            bs_mma<KIND>(d_tmem, adesc + uint64_t(kk * 2), bdesc + uint64_t(kk * 2), bs_idesc<KIND, TW * BN>(sfid),
+                         sfa, sfb, (kb | kk) != 0 ? 1u : 0u);
           }
           tc_commit(smem_u32(&c.empty[stage]));
           if (++stage == L::STAGES) { stage = 0; ph ^= 1u; }
