@@ -461,8 +461,8 @@ dmoe_status dmoe_quantize_nvfp4(const void* x, int rows, int cols, uint8_t* pack
  * are bitwise identical for any num_ctas and any stream; device-side errors
  * (offsets, row_src) go to the workspace status word as in
  * moe_grouped_gemm_dprob.  Tiles run on single CTAs: MXFP8 with an even
- * number of 128-column slots (N % 256 == 0) uses 128 x 256 tiles (the A
- * operand shared by the two slots' MMAs), otherwise 128 x 128; both give the
+ * number of 128-column slots (N % 256 == 0) uses 128 x 256 tiles (one
+ * N = 256 MMA per step over both slots), otherwise 128 x 128; both give the
  * same bits, and launch->flags = DMOE_LAUNCH_NARROW_TILES forces 128 x 128.
  * Other flags are ignored.
  */
