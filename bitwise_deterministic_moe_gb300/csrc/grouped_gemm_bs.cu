@@ -101,13 +101,21 @@ static_assert(BN == SLOT, "one tile is one slot");
 //          (16 with the 4-column alignment), one 256-column accumulator
 //          pair, and four stages: the epilogue stores from registers, so it
 //          needs no staging buffers.
+// MXFP8 scale boxes live outside the stages, in a ring of two slots: a box
+// holds 16 bytes of each row -- the words of four consecutive stages -- so it
+// is loaded once per group of four stages, and the transposer, which frees
+// the slot after the group's last stage, has three of the four stages' scale
+// blocks written before their operands land.  NVFP4 boxes (one stage's four
+// words) stay in the stage.
 template <int KIND, int TW>
 struct Layout {
   static_assert(TW == 1 || (TW == 2 && KIND == 0), "two-slot tiles are MXFP8 only");
+  static constexpr bool BOX_RING = KIND == 0;
   static constexpr int OFF_B = A_BYTES;                  // B box of slot h at OFF_B + h * B_BYTES
-  static constexpr int OFF_SFA_BOX = A_BYTES + TW * B_BYTES;
-  static constexpr int OFF_SFB_BOX = OFF_SFA_BOX + SFBOX_BYTES;   // slot h at + h * SFBOX_BYTES
-  static constexpr int OFF_SFA_BLK = OFF_SFB_BOX + TW * SFBOX_BYTES;
+  static constexpr int BOXES_BYTES = (1 + TW) * SFBOX_BYTES;   // the A box, then the B box (slot h at + h * SFBOX_BYTES)
+  static constexpr int OFF_SFA_BOX = A_BYTES + TW * B_BYTES;   // in the stage (NVFP4) or a ring slot (MXFP8, offset 0)
+  static constexpr int OFF_SFB_BOX = OFF_SFA_BOX + SFBOX_BYTES;
+  static constexpr int OFF_SFA_BLK = A_BYTES + TW * B_BYTES + (BOX_RING ? 0 : BOXES_BYTES);
   static constexpr int SRC_BYTES = KIND == 0 ? SFBLK_BYTES : SF256_BYTES;
   static constexpr int OFF_SFB_BLK = OFF_SFA_BLK + (KIND == 0 ? 1 : 2) * SRC_BYTES;   // slot h at + h * SRC_BYTES
   static constexpr int STAGE_BYTES = ((OFF_SFB_BLK + TW * (KIND == 0 ? 1 : 2) * SRC_BYTES) + 1023) / 1024 * 1024;
@@ -117,7 +125,10 @@ struct Layout {
   static constexpr int SF0 = ACC * TW * BN;              // first scale column
   static_assert(SF0 + STAGES * SF_COLS_STAGE <= TMEM_COLS, "tensor memory");
   static constexpr int STAGING = TW == 1 ? EPI_WARPS * STG_BYTES : 0;   // per-warp TMA store staging
-  static constexpr size_t SMEM = 1024 + size_t(STAGES) * STAGE_BYTES + size_t(STAGING) + 1024;
+  static constexpr int OFF_RING = STAGES * STAGE_BYTES + STAGING;       // 1024-byte aligned
+  static constexpr int RING_BYTES = BOX_RING ? 2 * BOXES_BYTES : 0;
+  static_assert(OFF_RING % 1024 == 0 && BOXES_BYTES % 1024 == 0, "TMA box destinations");
+  static constexpr size_t SMEM = 1024 + size_t(OFF_RING) + size_t(RING_BYTES) + 1024;
   static_assert(SMEM <= 232448, "dynamic shared memory above the 227 KB a CTA may use");
 };
 constexpr int MAX_STAGES = 5;
@@ -129,6 +140,8 @@ struct alignas(16) Ctrl {
   uint64_t sfin[MAX_STAGES];   // scale boxes landed
   uint64_t sfrdy[MAX_STAGES];  // scale blocks written by the transposer
   uint64_t empty[MAX_STAGES];  // the stage's MMAs and scale copies are done
+  uint64_t bxfull[2];          // MXFP8: a ring slot's scale boxes landed
+  uint64_t bxempty[2];         // MXFP8: the transposer is done with a ring slot
   uint64_t acc_full[ACC_BUFS];
   uint64_t acc_empty[ACC_BUFS];
   uint64_t mma_done;
@@ -248,8 +261,9 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   using L = Layout<KIND, TW>;
-  Ctrl& c = *reinterpret_cast<Ctrl*>(base + size_t(L::STAGES) * L::STAGE_BYTES + size_t(L::STAGING));
+  Ctrl& c = *reinterpret_cast<Ctrl*>(base + size_t(L::OFF_RING) + size_t(L::RING_BYTES));
   const uint32_t stage0 = smem_u32(base);
+  const uint32_t ring0 = stage0 + uint32_t(L::OFF_RING);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -262,6 +276,10 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
       mbar_init(smem_u32(&c.sfin[s]), 1);
       mbar_init(smem_u32(&c.sfrdy[s]), 1);
       mbar_init(smem_u32(&c.empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&c.bxfull[b]), 1);
+      mbar_init(smem_u32(&c.bxempty[b]), 1);
     }
     for (int b = 0; b < L::ACC; ++b) {
       mbar_init(smem_u32(&c.acc_full[b]), 1);
@@ -297,6 +315,7 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
     if (lane == 0) {
       // ------------------------------------------------ TMA producer
       int issued_total = 0;
+      int groups_issued = 0;   // MXFP8 scale-box loads, two ring slots in turn
       int stage = 0;
       uint32_t ph = 0;
       for (int qi = 0;; ++qi) {
@@ -309,6 +328,12 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
         bool ok = true;
         for (int kb = 0; kb < p.KB; ++kb) {
           if (!mbar_wait(smem_u32(&c.empty[stage]), ph ^ 1u, &c.abort, p.status, p.wait_ns)) { ok = false; break; }
+          // a group's ring slot is free once the transposer is done with the
+          // group two back (waited for before anything is issued, so that the
+          // drain below counts every copy in flight)
+          if (L::BOX_RING && (kb & 3) == 0 &&
+              !mbar_wait(smem_u32(&c.bxempty[groups_issued & 1]), uint32_t((groups_issued >> 1) & 1) ^ 1u, &c.abort,
+                         p.status, p.wait_ns)) { ok = false; break; }
           const uint32_t sa = stage0 + stage * L::STAGE_BYTES;
           const uint32_t full = smem_u32(&c.full[stage]);
           const uint32_t sfin = smem_u32(&c.sfin[stage]);
@@ -317,11 +342,23 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
           // B (and below its scales): one box of TW * 128 rows -- the tensor
           // maps' box height -- whose slot-h half lands at + h * B_BYTES
           tma_load_2d(sa + L::OFF_B, &tmap_b, full, kb * ROWB, brow);
-          // 16 bytes of scales per row: four stages' words (MXFP8) or this stage's four (NVFP4)
-          const int sx = KIND == kMxf8 ? 16 * (kb >> 2) : 16 * kb;
-          mbar_arrive_expect_tx(sfin, (1 + TW) * SFBOX_BYTES);
-          tma_load_2d(sa + L::OFF_SFA_BOX, &tmap_sfa, sfin, sx, tl.row0);
-          tma_load_2d(sa + L::OFF_SFB_BOX, &tmap_sfb, sfin, sx, brow);
+          // 16 bytes of scales per row: four stages' words (MXFP8, into a
+          // ring slot once per group) or this stage's four (NVFP4)
+          if (L::BOX_RING) {
+            if ((kb & 3) == 0) {
+              const int b = groups_issued & 1;
+              const uint32_t slot = ring0 + uint32_t(b * L::BOXES_BYTES);
+              const uint32_t bx = smem_u32(&c.bxfull[b]);
+              mbar_arrive_expect_tx(bx, L::BOXES_BYTES);
+              tma_load_2d(slot, &tmap_sfa, bx, 16 * (kb >> 2), tl.row0);
+              tma_load_2d(slot + SFBOX_BYTES, &tmap_sfb, bx, 16 * (kb >> 2), brow);
+              ++groups_issued;
+            }
+          } else {
+            mbar_arrive_expect_tx(sfin, (1 + TW) * SFBOX_BYTES);
+            tma_load_2d(sa + L::OFF_SFA_BOX, &tmap_sfa, sfin, 16 * kb, tl.row0);
+            tma_load_2d(sa + L::OFF_SFB_BOX, &tmap_sfb, sfin, 16 * kb, brow);
+          }
           ++issued_total;
           if (++stage == L::STAGES) { stage = 0; ph ^= 1u; }
         }
@@ -332,7 +369,13 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
         const int n = (issued_total - s + L::STAGES - 1) / L::STAGES;
         if (n > 0) {
           mbar_wait_drain(smem_u32(&c.full[s]), uint32_t(n - 1) & 1u, p.wait_ns / 4);
-          mbar_wait_drain(smem_u32(&c.sfin[s]), uint32_t(n - 1) & 1u, p.wait_ns / 4);
+          if (!L::BOX_RING) mbar_wait_drain(smem_u32(&c.sfin[s]), uint32_t(n - 1) & 1u, p.wait_ns / 4);
+        }
+      }
+      if (L::BOX_RING) {
+        for (int b = 0; b < 2; ++b) {
+          const int n = (groups_issued - b + 1) / 2;
+          if (n > 0) mbar_wait_drain(smem_u32(&c.bxfull[b]), uint32_t(n - 1) & 1u, p.wait_ns / 4);
         }
       }
     }
@@ -409,8 +452,13 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
     //        the scale of tile row 32c + j for that MMA in every lane quarter,
     //        as the replicating .32x128b.warpx4 copy lays it out.  Lane j owns
     //        tile rows j, 32 + j, 64 + j, 96 + j.
+    // MXFP8: the boxes of a group of four stages sit in ring slot g % 2; the
+    // stage's block area is free once the stage's previous MMAs are done
+    // (the producer's wait, on the same barrier), which is usually long
+    // before the stage's operands land.
     int stage = 0;
     uint32_t ph = 0;
+    int groups_done = 0;
     for (int qi = 0;; ++qi) {
       const int qs = qi % TQ;
       if (!warp_wait(smem_u32(&c.tq_full[qs]), uint32_t((qi / TQ) & 1), &c.abort, p.status, lane, p.wait_ns)) break;
@@ -420,12 +468,23 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
       if (cur < 0) break;
       bool ok = true;
       for (int kb = 0; kb < p.KB; ++kb) {
-        if (!warp_wait(smem_u32(&c.sfin[stage]), ph, &c.abort, p.status, lane, p.wait_ns)) { ok = false; break; }
+        uint32_t boxes;
+        if (L::BOX_RING) {
+          const int b = groups_done & 1;
+          if ((kb & 3) == 0 &&
+              !warp_wait(smem_u32(&c.bxfull[b]), uint32_t((groups_done >> 1) & 1), &c.abort, p.status, lane,
+                         p.wait_ns)) { ok = false; break; }
+          if (!warp_wait(smem_u32(&c.empty[stage]), ph ^ 1u, &c.abort, p.status, lane, p.wait_ns)) { ok = false; break; }
+          boxes = ring0 + uint32_t(b * L::BOXES_BYTES);
+        } else {
+          if (!warp_wait(smem_u32(&c.sfin[stage]), ph, &c.abort, p.status, lane, p.wait_ns)) { ok = false; break; }
+          boxes = stage0 + stage * L::STAGE_BYTES + L::OFF_SFA_BOX;
+        }
         const uint32_t sa = stage0 + stage * L::STAGE_BYTES;
 #pragma unroll
         for (int op = 0; op < 1 + TW; ++op) {
           // op 0: A; op 1 + h: B of slot h
-          const uint32_t box = sa + (op == 0 ? L::OFF_SFA_BOX : L::OFF_SFB_BOX + (op - 1) * SFBOX_BYTES);
+          const uint32_t box = boxes + (op == 0 ? 0u : uint32_t(SFBOX_BYTES + (op - 1) * SFBOX_BYTES));
           const uint32_t blk = sa + (op == 0 ? L::OFF_SFA_BLK : L::OFF_SFB_BLK + (op - 1) * L::SRC_BYTES);
           uint4 r[4];
 #pragma unroll
@@ -455,6 +514,11 @@ grouped_gemm_bs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_
         fence_proxy_async_smem();   // the generic-proxy block writes, before the tensor core's copy reads them
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&c.sfrdy[stage]));
+        if (L::BOX_RING && ((kb & 3) == 3 || kb == p.KB - 1)) {
+          // every lane has read the group's boxes (the barrier above): the slot can be reloaded
+          if (lane == 0) mbar_arrive(smem_u32(&c.bxempty[groups_done & 1]));
+          ++groups_done;
+        }
         if (++stage == L::STAGES) { stage = 0; ph ^= 1u; }
       }
       if (!ok) break;
