@@ -373,8 +373,9 @@ def block_scaled_measure(api, cfg, X, W, G, off, src, ws, timed, iters):
                      "peak_source": f"measured bf16 burst x {ratio:g} (nominal dense ratio)",
                      "tensor_frac": tf / peak, "algorithmic_bytes": b, "achieved_gbs": b / (ms * 1e-3) / 1e9,
                      "hbm_frac": b / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
-                     "kernel": ("grouped_gemm_bs_kernel: 128x256 tiles (two slots sharing the A operand), one "
-                                "accumulator pair drained to bf16 registers, four stages, one CTA per SM"
+                     "kernel": ("grouped_gemm_bs_kernel: 128x256 tiles (one N=256 MMA per step over two slots), "
+                                "scale boxes in a ring loaded once per four stages, one accumulator pair drained "
+                                "to bf16 registers, four stages, one CTA per SM"
                                 if kind == "mxfp8" and N % 256 == 0 else
                                 "grouped_gemm_bs_kernel: 128x128 tiles, two epilogue groups on alternate tiles, "
                                 "three accumulators, one CTA per SM")}
